@@ -1,0 +1,301 @@
+"""Pins for the CPU oracle: facts the mathematics fixes, independent of the
+oracle's own code.  CPU only.
+
+What the oracle computes is the plain definition of softmax cross-entropy on
+the LM-head logits S = X W^T, mean over rows whose target is not the ignore
+index, with the exact gradients (Liger-Kernel project overview,
+"Método de API de Baixo Nível" and "Cálculo Preciso").  Each pin below is
+chosen so that a plausible slip (a dropped term, a sign, an index, a
+transposed operand, the wrong normaliser) fails at least one of them.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from flce_synth import WORKLOADS, make_case, make_inputs
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")))
+IGN = -100
+
+
+def _rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+# --------------------------------------------------------------------------- W = 0
+@pytest.mark.parametrize("V", [2, 256, 32000, 128256, 152064])
+def test_zero_weight_loss_is_log_V(V):
+    """W = 0: every logit is 0, so each row's loss is log V exactly."""
+    N, H = 3, 8
+    X = _rand((N, H), 1)
+    W = np.zeros((V, H))
+    t = np.array([0, V - 1, V // 2], dtype=np.int64)
+    r = oracle.flce(X, W, t, grads=(V <= 256))
+    ref = GOLDEN["log_V"][str(V)]
+    assert abs(r["loss"] - ref) <= 4e-16 * ref
+    assert abs(ref - math.log(V)) <= 4e-16 * ref
+    np.testing.assert_allclose(r["lse"], ref, rtol=4e-16)
+
+
+def test_zero_weight_gradients_closed_form():
+    """W = 0: dX = 0 and dW_j = (1/n) sum_valid (1/V - [j = t_i]) x_i."""
+    N, H, V = 7, 5, 11
+    X = _rand((N, H), 2)
+    W = np.zeros((V, H))
+    t = np.array([3, IGN, 0, 10, 3, IGN, 7], dtype=np.int64)
+    r = oracle.flce(X, W, t, IGN)
+    n = 5
+    assert r["n_valid"] == n
+    np.testing.assert_array_equal(r["dX"], 0.0)
+    expect = np.zeros((V, H))
+    for i in range(N):
+        if t[i] == IGN:
+            continue
+        expect += np.outer(np.full(V, 1.0 / V), X[i]) / n
+        expect[t[i]] -= X[i] / n
+    np.testing.assert_allclose(r["dW"], expect, rtol=1e-13, atol=1e-15)
+
+
+# ------------------------------------------------------------------ G = dW^T with X = I
+def test_identity_input_exposes_G_against_scipy_softmax():
+    """X = I (N = H) makes dW = G^T, so G is visible: each valid row sums to 0,
+    ignored rows are exactly 0, and G = (softmax(S) - onehot)/n_valid with the
+    softmax taken from scipy."""
+    from scipy.special import softmax
+    N = H = 6
+    V = 9
+    X = np.eye(N)
+    W = _rand((V, H), 3, 2.0)
+    t = np.array([4, IGN, 8, 0, 4, IGN], dtype=np.int64)
+    r = oracle.flce(X, W, t, IGN)
+    G = r["dW"].T
+    assert G.shape == (N, V)
+    np.testing.assert_allclose(G.sum(axis=1), 0.0, atol=1e-15)
+    np.testing.assert_array_equal(G[t == IGN], 0.0)
+    S = W.T  # S_ij = sum_h I_ih W_jh = W_ji
+    P = softmax(S, axis=1)
+    n = int((t != IGN).sum())
+    for i in range(N):
+        if t[i] == IGN:
+            continue
+        e = P[i].copy()
+        e[t[i]] -= 1.0
+        np.testing.assert_allclose(G[i], e / n, rtol=1e-12, atol=1e-16)
+    # dX_i = sum_j G_ij w_j  -> with X = I the same G gives dX = G W
+    np.testing.assert_allclose(r["dX"], G @ W, rtol=1e-12, atol=1e-15)
+
+
+# --------------------------------------------------------------------------- V = 2
+def test_two_class_softplus():
+    """V = 2: row loss = softplus(S_other - S_target) = logaddexp(0, d)."""
+    N, H = 9, 4
+    X = _rand((N, H), 4)
+    W = _rand((2, H), 5)
+    t = np.array([0, 1, 1, 0, IGN, 1, 0, 0, 1], dtype=np.int64)
+    r = oracle.flce(X, W, t, IGN)
+    S = X @ W.T
+    for i in range(N):
+        if t[i] == IGN:
+            assert r["loss_rows"][i] == 0.0
+            continue
+        d = S[i, 1 - t[i]] - S[i, t[i]]
+        assert abs(r["loss_rows"][i] - np.logaddexp(0.0, d)) <= 1e-13
+    valid = t != IGN
+    assert abs(r["loss"] - r["loss_rows"][valid].mean()) <= 1e-14
+
+
+# ------------------------------------------------------------------------ invariants
+def test_loss_nonnegative_and_rows_sum_zero():
+    X, W, t = make_case(33, 24, 70, "fp32", seed=11, w_std=0.5, ignore_num=10)
+    r = oracle.flce(X, W, t, IGN)
+    assert r["loss"] >= 0.0
+    assert (r["loss_rows"] >= 0.0).all()
+    # sum_j dW_j = sum_i (sum_j G_ij) x_i = 0
+    assert np.abs(r["dW"].sum(axis=0)).max() <= 1e-14 * np.abs(r["dW"]).max() * 70
+    # rows of dX for ignored targets are exactly zero
+    ign = (t == IGN).numpy()
+    assert ign.sum() == 3
+    np.testing.assert_array_equal(r["dX"][ign], 0.0)
+
+
+def test_shift_invariance():
+    """W + 1 b^T adds x_i.b to every logit of row i: softmax, loss and dW are
+    unchanged, and dX = G (W + 1 b^T) = G W because each row of G sums to 0."""
+    N, H, V = 6, 5, 13
+    X = _rand((N, H), 6)
+    W = _rand((V, H), 7)
+    b = _rand((H,), 8)
+    t = np.array([1, 12, IGN, 5, 5, 0], dtype=np.int64)
+    a = oracle.flce(X, W, t, IGN)
+    s = oracle.flce(X, W + b[None, :], t, IGN)
+    assert abs(a["loss"] - s["loss"]) <= 1e-13
+    np.testing.assert_allclose(s["dW"], a["dW"], rtol=1e-11, atol=1e-14)
+    np.testing.assert_allclose(s["dX"], a["dX"], rtol=1e-11, atol=1e-14)
+
+
+def test_duplicated_batch():
+    """Repeating the batch keeps the mean loss and dW, and halves each dX row
+    (the normaliser doubles): pins the 1/n_valid scaling."""
+    N, H, V = 5, 7, 10
+    X = _rand((N, H), 9)
+    W = _rand((V, H), 10)
+    t = np.array([2, IGN, 9, 0, 4], dtype=np.int64)
+    a = oracle.flce(X, W, t, IGN)
+    d = oracle.flce(np.vstack([X, X]), W, np.concatenate([t, t]), IGN)
+    assert d["n_valid"] == 2 * a["n_valid"]
+    assert abs(d["loss"] - a["loss"]) <= 1e-14
+    np.testing.assert_allclose(d["dW"], a["dW"], rtol=1e-12, atol=1e-16)
+    np.testing.assert_allclose(d["dX"][:N], a["dX"] / 2, rtol=1e-12, atol=1e-16)
+
+
+def test_all_ignored_and_empty():
+    """Reading taken: no valid row gives loss 0 and zero gradients."""
+    N, H, V = 4, 3, 5
+    X = _rand((N, H), 12)
+    W = _rand((V, H), 13)
+    t = np.full(N, IGN, dtype=np.int64)
+    r = oracle.flce(X, W, t, IGN)
+    assert r["loss"] == 0.0 and r["n_valid"] == 0
+    np.testing.assert_array_equal(r["dX"], 0.0)
+    np.testing.assert_array_equal(r["dW"], 0.0)
+    e = oracle.flce(np.zeros((0, H)), W, np.zeros(0, dtype=np.int64), IGN)
+    assert e["loss"] == 0.0 and e["n_valid"] == 0 and e["dW"].shape == (V, H)
+
+
+def test_bad_target_rejected():
+    X = _rand((2, 3), 14)
+    W = _rand((4, 3), 15)
+    with pytest.raises(oracle.OracleError):
+        oracle.flce(X, W, np.array([0, 4]), IGN)
+    with pytest.raises(oracle.OracleError):
+        oracle.flce(X, W, np.array([-1, 0]), IGN)
+    # a custom ignore index is honoured
+    r = oracle.flce(X, W, np.array([7, 1]), 7)
+    assert r["n_valid"] == 1
+
+
+# ----------------------------------------------------------------------- brute force
+def test_brute_force_every_target_assignment():
+    """N = 3, V = 4, H = 2: every assignment of targets (including ignored rows)
+    against a 50-digit mpmath evaluation of the unshifted definition; gradients
+    against 50-digit central differences of that same evaluation."""
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 50
+    N, H, V = 3, 2, 4
+    X = np.round(_rand((N, H), 16), 3)
+    W = np.round(_rand((V, H), 17), 3)
+
+    def mp_loss(Xm, Wm, t):
+        tot, n = mp.mpf(0), 0
+        for i in range(N):
+            if t[i] == IGN:
+                continue
+            s = [mp.fsum(Xm[i][h] * Wm[j][h] for h in range(H)) for j in range(V)]
+            tot += mp.log(mp.fsum(mp.exp(v) for v in s)) - s[t[i]]
+            n += 1
+        return tot / n if n else mp.mpf(0)
+
+    Xm = [[mp.mpf(float(v)) for v in row] for row in X]
+    Wm = [[mp.mpf(float(v)) for v in row] for row in W]
+    eps = mp.mpf(10) ** -20
+    for assign in itertools.product([IGN, 0, 1, 2, 3], repeat=N):
+        t = np.array(assign, dtype=np.int64)
+        r = oracle.flce(X, W, t, IGN)
+        ref = mp_loss(Xm, Wm, t)
+        assert abs(r["loss"] - float(ref)) <= 1e-14 * max(1.0, abs(float(ref)))
+        if assign not in [(0, 1, 2), (IGN, 3, 3), (2, IGN, IGN), (IGN, IGN, IGN)]:
+            continue
+        for (i, h) in itertools.product(range(N), range(H)):
+            Xp = [row[:] for row in Xm]; Xp[i][h] += eps
+            Xn = [row[:] for row in Xm]; Xn[i][h] -= eps
+            g = (mp_loss(Xp, Wm, t) - mp_loss(Xn, Wm, t)) / (2 * eps)
+            assert abs(r["dX"][i, h] - float(g)) <= 1e-14
+        for (j, h) in itertools.product(range(V), range(H)):
+            Wp = [row[:] for row in Wm]; Wp[j][h] += eps
+            Wn = [row[:] for row in Wm]; Wn[j][h] -= eps
+            g = (mp_loss(Xm, Wp, t) - mp_loss(Xm, Wn, t)) / (2 * eps)
+            assert abs(r["dW"][j, h] - float(g)) <= 1e-14
+
+
+# ---------------------------------------------------------------- finite differences
+def test_finite_differences_worked_example():
+    """Central differences of the oracle's loss against every entry of dX and
+    dW on the overview's worked example (N=4, H=128, V=256, float32 inputs
+    widened to double)."""
+    w = WORKLOADS["tiny_worked_4x128x256_fp32"]
+    X, W, t = make_inputs(w)
+    X = X.double().numpy().copy()
+    W = W.double().numpy().copy()
+    r = oracle.flce(X, W, t, IGN)
+    h = 1e-5
+    # dX: every entry
+    fd = np.zeros_like(X)
+    for idx in np.ndindex(X.shape):
+        x0 = X[idx]
+        X[idx] = x0 + h; lp = oracle.flce(X, W, t, IGN, grads=False)["loss"]
+        X[idx] = x0 - h; lm = oracle.flce(X, W, t, IGN, grads=False)["loss"]
+        X[idx] = x0
+        fd[idx] = (lp - lm) / (2 * h)
+    assert np.abs(fd - r["dX"]).max() <= 1e-8 * np.abs(r["dX"]).max() + 1e-10
+    # dW: every entry; perturbing W[j, k] moves only logit column j
+    fdw = np.zeros_like(W)
+    for idx in np.ndindex(W.shape):
+        w0 = W[idx]
+        W[idx] = w0 + h; lp = oracle.flce(X, W, t, IGN, grads=False)["loss"]
+        W[idx] = w0 - h; lm = oracle.flce(X, W, t, IGN, grads=False)["loss"]
+        W[idx] = w0
+        fdw[idx] = (lp - lm) / (2 * h)
+    assert np.abs(fdw - r["dW"]).max() <= 1e-8 * np.abs(r["dW"]).max() + 1e-10
+
+
+# ------------------------------------------------------------- library special case
+@pytest.mark.parametrize("case", [
+    dict(N=4, H=128, V=256, dtype="fp32", ignore_num=0, seed=1000),
+    dict(N=37, H=40, V=301, dtype="bf16", ignore_num=20, seed=3),
+    dict(N=64, H=96, V=1000, dtype="bf16", ignore_num=5, seed=4, t_dist="zipf"),
+])
+def test_against_torch_float64_autograd(case):
+    """torch float64 F.linear + F.cross_entropy(ignore_index, mean) + autograd."""
+    args = dict(case)
+    X, W, t = make_case(args.pop("N"), args.pop("H"), args.pop("V"), **args)
+    r = oracle.flce(X, W, t, IGN)
+    Xd = X.double().requires_grad_(True)
+    Wd = W.double().requires_grad_(True)
+    loss = torch.nn.functional.cross_entropy(torch.nn.functional.linear(Xd, Wd), t,
+                                             ignore_index=IGN, reduction="mean")
+    loss.backward()
+    assert abs(r["loss"] - loss.item()) <= 1e-12 * abs(loss.item())
+    np.testing.assert_allclose(r["dX"], Xd.grad.numpy(), rtol=1e-9, atol=1e-15)
+    np.testing.assert_allclose(r["dW"], Wd.grad.numpy(), rtol=1e-9, atol=1e-15)
+
+
+def test_row_and_vocab_subsets_match_full():
+    X, W, t = make_case(29, 16, 77, "bf16", seed=21, ignore_num=10, w_std=0.3)
+    full = oracle.flce(X, W, t, IGN)
+    rows = [0, 5, 28, 13]
+    sub = oracle.flce_rows(X, W, t, rows, IGN)
+    assert sub["n_valid"] == full["n_valid"]
+    np.testing.assert_allclose(sub["lse"], full["lse"][rows], rtol=1e-15)
+    np.testing.assert_allclose(sub["loss_rows"], full["loss_rows"][rows], rtol=1e-15)
+    np.testing.assert_allclose(sub["dX"], full["dX"][rows], rtol=1e-13, atol=1e-18)
+    voc = [76, 0, 40]
+    dw = oracle.flce_dw_rows(X, W, t, voc, IGN)
+    np.testing.assert_allclose(dw, full["dW"][voc], rtol=1e-13, atol=1e-18)
+
+
+# ------------------------------------------------------------------ generator counts
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_workload_valid_counts(name):
+    """n_valid = N - floor(p N) exactly, from the generator's recipe."""
+    from flce_synth import targets
+    w = WORKLOADS[name]
+    t = targets(w.N, w.V, w.t_dist, w.seed, w.ignore_num, 100, w.ignore_index)
+    assert oracle.count_valid(t, IGN) == GOLDEN["ignored_counts"][name]
+    valid = t[t != IGN]
+    assert valid.min() >= 0 and valid.max() < w.V
