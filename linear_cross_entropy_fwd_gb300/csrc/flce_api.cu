@@ -1,0 +1,650 @@
+// flce_api.cu -- host side of libflce: argument checks, the workspace plan,
+// TMA descriptors, the launch sequence and the extern "C" entry points.
+//
+// Launch sequence of one call (all on the caller's stream, no host sync
+// unless the call is synchronous):
+//   1  logits_lse   pass 1: S tiles = X W^T in TMEM; per-tile row max/sum-exp
+//   2  combine      lse_i, row loss, mean loss, n_valid, gradient scale
+//   for each vocabulary chunk c = [c0, c0 + vc):
+//   3  logits_grad  pass 2: recompute S[:, c] in TMEM, G_c = (softmax - onehot) * scale
+//   4  dw           dW[c] = G_c^T X            (fp32, written once)
+//   5  dx           dX_acc (+)= G_c W[c]       (fp32, TMA add at L2 after chunk 0)
+//   6  convert      dX_acc -> dX (bf16 inputs only; fp32 inputs accumulate in dX)
+// fp32 inputs (tf32 products) feed steps 4 and 5 K-major transposed copies
+// X^T, G_c^T and W[c]^T made by a transpose kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/flce.h"
+#include "launch.h"
+
+namespace flce {
+namespace {
+
+thread_local char g_last_error[512] = {0};
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  set_error("%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+  return FLCE_ERR_CUDA;
+}
+
+#define FLCE_CUDA(call)                                 \
+  do {                                                  \
+    cudaError_t e_ = (call);                            \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+  } while (0)
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ----------------------------------------------------------- device cache
+struct DeviceInfo {
+  int sms = 0;
+  bool ok_arch = false;
+  bool prepared_bf16 = false;
+  bool prepared_fp32 = false;
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+int device_info(int dtype, DeviceInfo* out) {
+  int dev = 0;
+  FLCE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_error("device ordinal %d out of range", dev);
+    return FLCE_ERR_ARG;
+  }
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (d.sms == 0) {
+    int major = 0, minor = 0, sms = 0;
+    FLCE_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+    FLCE_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+    FLCE_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    d.ok_arch = (major == 10 && minor == 3);
+    d.sms = sms;
+    if (!d.ok_arch) {
+      set_error("device %d has compute capability %d.%d; libflce is built for 10.3 (sm_103a)",
+                dev, major, minor);
+    }
+  }
+  if (!d.ok_arch) return FLCE_ERR_ARCH;
+  if (dtype == FLCE_BF16 && !d.prepared_bf16) {
+    FLCE_CUDA(gemm_prepare_bf16());
+    d.prepared_bf16 = true;
+  }
+  if (dtype == FLCE_FP32 && !d.prepared_fp32) {
+    FLCE_CUDA(gemm_prepare_fp32());
+    d.prepared_fp32 = true;
+  }
+  *out = d;
+  return FLCE_OK;
+}
+
+// ------------------------------------------------------------ TMA encode
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2D map over a row-major [rows, cols] matrix: dim0 = cols (contiguous).
+int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elt, uint64_t cols,
+             uint64_t rows, uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows,
+             const char* what) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return FLCE_ERR_CUDA;
+  }
+  if (box_cols * static_cast<uint32_t>(elt) != 128u || box_rows == 0 || box_rows > 256) {
+    set_error("internal: bad TMA box for %s", what);
+    return FLCE_ERR_ARG;
+  }
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled(%s) failed with CUresult %d (cols=%llu rows=%llu pitch=%llu)",
+              what, static_cast<int>(r), static_cast<unsigned long long>(cols),
+              static_cast<unsigned long long>(rows), static_cast<unsigned long long>(pitch_bytes));
+    return FLCE_ERR_CUDA;
+  }
+  return FLCE_OK;
+}
+
+// ------------------------------------------------------------------ plan
+struct Plan {
+  int64_t N = 0, H = 0, V = 0;
+  int dtype = FLCE_BF16;
+  int elt = 2;
+  bool grads = false;
+  int64_t num_vblk = 0;   // vocabulary tiles of BN columns
+  int64_t Vc = 0;         // chunk width (multiple of BN)
+  int64_t num_chunks = 0;
+  int cgrid = 1;          // combine blocks
+  int64_t Np = 0;         // N rounded up to 4 (row pitch of the fp32 transposes)
+  size_t off_sc = 0, off_blk_loss = 0, off_blk_cnt = 0, off_lse2 = 0, off_st = 0,
+         off_partial = 0, off_dxacc = 0, off_xt = 0, off_G = 0, off_gt = 0, off_wt = 0,
+         total = 0;
+};
+
+size_t fixed_bytes(Plan& p) {
+  size_t o = 0;
+  p.off_sc = o;
+  o += align_up(sizeof(Scalars), 256);
+  p.off_blk_loss = o;
+  o += align_up(static_cast<size_t>(p.cgrid) * sizeof(double), 256);
+  p.off_blk_cnt = o;
+  o += align_up(static_cast<size_t>(p.cgrid) * sizeof(int64_t), 256);
+  p.off_lse2 = o;
+  o += align_up(static_cast<size_t>(p.N) * 4, 256);
+  p.off_st = o;
+  o += align_up(static_cast<size_t>(p.N) * 4, 256);
+  p.off_partial = o;
+  o += align_up(static_cast<size_t>(p.num_vblk) * static_cast<size_t>(p.N) * 4, 256);
+  p.off_dxacc = o;
+  if (p.grads && p.dtype == FLCE_BF16)
+    o += align_up(static_cast<size_t>(p.N) * static_cast<size_t>(p.H) * 4, 256);
+  p.off_xt = o;
+  if (p.grads && p.dtype == FLCE_FP32)
+    o += align_up(static_cast<size_t>(p.H) * static_cast<size_t>(p.Np) * 4, 256);
+  p.off_G = o;
+  return o;
+}
+
+// budget: bytes the plan may use (0 = N*V*4/16).  Returns FLCE_OK or an error.
+int make_plan(Plan* out, int64_t N, int64_t H, int64_t V, bool grads, const flce_opts& o,
+              size_t budget) {
+  Plan p;
+  p.N = N;
+  p.H = H;
+  p.V = V;
+  p.dtype = o.dtype;
+  p.elt = (o.dtype == FLCE_FP32) ? 4 : 2;
+  p.grads = grads;
+  p.num_vblk = (V + BN - 1) / BN;
+  p.cgrid = combine_grid(N);
+  p.Np = (N + 3) / 4 * 4;
+  const size_t fixed = fixed_bytes(p);
+  if (grads && N > 0) {
+    const int64_t vpad = p.num_vblk * BN;
+    int64_t Vc;
+    if (o.vocab_chunk > 0) {
+      if (o.vocab_chunk % BN != 0) {
+        set_error("vocab_chunk must be a positive multiple of %d", BN);
+        return FLCE_ERR_ARG;
+      }
+      Vc = o.vocab_chunk;
+    } else {
+      if (budget == 0) budget = static_cast<size_t>(N) * static_cast<size_t>(V) * 4 / 16;
+      size_t per_col = static_cast<size_t>(N) * p.elt;  // G chunk column
+      if (p.dtype == FLCE_FP32)                            // + G^T and W^T columns
+        per_col += static_cast<size_t>(p.Np) * 4 + static_cast<size_t>(H) * 4;
+      const size_t avail = budget > fixed ? budget - fixed : 0;
+      Vc = static_cast<int64_t>(avail / per_col) / BN * BN;
+      if (Vc < BN) Vc = BN;
+    }
+    if (Vc > vpad) Vc = vpad;
+    p.Vc = Vc;
+    p.num_chunks = (V + Vc - 1) / Vc;
+    size_t o = fixed + align_up(static_cast<size_t>(N) * static_cast<size_t>(Vc) * p.elt, 256);
+    p.off_gt = o;
+    p.off_wt = o;
+    if (p.dtype == FLCE_FP32) {
+      o += align_up(static_cast<size_t>(Vc) * static_cast<size_t>(p.Np) * 4, 256);
+      p.off_wt = o;
+      o += align_up(static_cast<size_t>(H) * static_cast<size_t>(Vc) * 4, 256);
+    }
+    p.total = o;
+  } else {
+    p.total = fixed;
+  }
+  *out = p;
+  return FLCE_OK;
+}
+
+int check_args(const void* X, const void* W, const int64_t* target, int64_t N, int64_t H,
+               int64_t V, const flce_opts& o) {
+  if (N < 0 || H <= 0 || V <= 0) {
+    set_error("sizes must satisfy N >= 0, H > 0, V > 0 (got N=%lld H=%lld V=%lld)",
+              static_cast<long long>(N), static_cast<long long>(H), static_cast<long long>(V));
+    return FLCE_ERR_ARG;
+  }
+  if (o.dtype != FLCE_BF16 && o.dtype != FLCE_FP32) {
+    set_error("unknown dtype %d", o.dtype);
+    return FLCE_ERR_ARG;
+  }
+  if (N > (int64_t{1} << 31) - BM || V > (int64_t{1} << 31) - BN || H > (int64_t{1} << 24)) {
+    set_error("size too large (N < 2^31, V < 2^31, H <= 2^24)");
+    return FLCE_ERR_ARG;
+  }
+  if (!W || (N > 0 && (!X || !target))) {
+    set_error("null input pointer");
+    return FLCE_ERR_ARG;
+  }
+  const int elt = (o.dtype == FLCE_FP32) ? 4 : 2;
+  if ((H * elt) % 16 != 0) {
+    set_error("H * sizeof(element) = %lld is not a multiple of 16 bytes",
+              static_cast<long long>(H * elt));
+    return FLCE_ERR_ALIGN;
+  }
+  if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W)) & 15u) {
+    set_error("X and W must be 16-byte aligned");
+    return FLCE_ERR_ALIGN;
+  }
+  if (o.grad_scale != o.grad_scale) {
+    set_error("grad_scale is NaN");
+    return FLCE_ERR_ARG;
+  }
+  return FLCE_OK;
+}
+
+struct Tracer {
+  const flce_opts& o;
+  cudaStream_t s;
+  int32_t n = 0;
+  Tracer(const flce_opts& opts, cudaStream_t st) : o(opts), s(st) {}
+  int start() {
+    if (!o.trace_events || o.trace_capacity < 1) return FLCE_OK;
+    FLCE_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(o.trace_events[0]), s));
+    n = 1;
+    return FLCE_OK;
+  }
+  int after(int kind) {
+    if (!o.trace_events || n == 0 || n >= o.trace_capacity) return FLCE_OK;
+    FLCE_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(o.trace_events[n]), s));
+    if (o.trace_kinds) o.trace_kinds[n - 1] = kind;
+    ++n;
+    return FLCE_OK;
+  }
+  void finish() {
+    if (o.trace_count) *o.trace_count = n;
+  }
+};
+
+int grid_for(int64_t tiles, int sms) {
+  return static_cast<int>(tiles < sms ? tiles : sms);
+}
+
+// The whole path on device pointers.  `ws` holds at least plan.total bytes.
+int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
+             const int64_t* target, int64_t ignore_index, void* dX, float* dW, uint8_t* ws,
+             const flce_opts& o, cudaStream_t s) {
+  const int64_t N = P.N, H = P.H, V = P.V;
+  const int elt = P.elt;
+  const bool bf16 = (P.dtype == FLCE_BF16);
+  const CUtensorMapDataType dt =
+      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const int KE = 128 / elt;  // K elements per 128-byte stage
+  Scalars* sc = reinterpret_cast<Scalars*>(ws + P.off_sc);
+  float* lse2 = reinterpret_cast<float*>(ws + P.off_lse2);
+  float* st = reinterpret_cast<float*>(ws + P.off_st);
+  float* partial = reinterpret_cast<float*>(ws + P.off_partial);
+  int rc;
+  Tracer tr(o, s);
+
+  FLCE_CUDA(cudaMemsetAsync(sc, 0, sizeof(Scalars), s));
+  if ((rc = tr.start())) return rc;
+
+  // ---- pass 1 and combine
+  if (N > 0) {
+    CUtensorMap mX, mW;
+    if ((rc = make_map(&mX, X, dt, elt, H, N, H * elt, KE, BM, "X (K-major)"))) return rc;
+    if ((rc = make_map(&mW, W, dt, elt, H, V, H * elt, KE, BN, "W (K-major)"))) return rc;
+    GemmGrid g{};
+    g.num_m_blk = static_cast<int32_t>((N + BM - 1) / BM);
+    g.num_n_blk = static_cast<int32_t>(P.num_vblk);
+    g.num_k_blk = static_cast<int32_t>((H + KE - 1) / KE);
+    g.status = &sc->status;
+    RowLseParams rp{target, partial, st, N, V};
+    const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, D.sms);
+    FLCE_CUDA(bf16 ? launch_logits_lse_bf16(mX, mW, g, rp, grid, s)
+                   : launch_logits_lse_fp32(mX, mW, g, rp, grid, s));
+    if ((rc = tr.after(FLCE_TRACE_LOGITS_LSE))) return rc;
+  }
+  CombineParams cp{};
+  cp.partial = partial;
+  cp.num_vblk = static_cast<int32_t>(P.num_vblk);
+  cp.st = st;
+  cp.target = target;
+  cp.N = N;
+  cp.V = V;
+  cp.ignore_index = ignore_index;
+  cp.lse2 = lse2;
+  cp.lse_out = o.lse_out;
+  cp.loss_rows_out = o.loss_rows_out;
+  cp.blk_loss = reinterpret_cast<double*>(ws + P.off_blk_loss);
+  cp.blk_cnt = reinterpret_cast<int64_t*>(ws + P.off_blk_cnt);
+  cp.sc = sc;
+  cp.grad_scale = o.grad_scale;
+  cp.norm_count = o.norm_count;
+  cp.loss_out = o.loss_dev;
+  cp.nvalid_out = o.n_valid_dev;
+  FLCE_CUDA(launch_combine(cp, s));
+  if ((rc = tr.after(FLCE_TRACE_COMBINE))) return rc;
+
+  // ---- pass 2 and the gradient GEMMs, chunk by chunk over the vocabulary
+  if (P.grads) {
+    if (N == 0) {
+      FLCE_CUDA(cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * 4, s));
+    } else {
+      uint8_t* G = ws + P.off_G;
+      float* dxacc = bf16 ? reinterpret_cast<float*>(ws + P.off_dxacc) : static_cast<float*>(dX);
+      const int64_t Vc = P.Vc, Np = P.Np;
+      float* Xt = reinterpret_cast<float*>(ws + P.off_xt);
+      float* Gt = reinterpret_cast<float*>(ws + P.off_gt);
+      float* Wt = reinterpret_cast<float*>(ws + P.off_wt);
+      // A/B maps of the dW GEMM (mA4, mB4) and of the dX GEMM (mA5, mB5)
+      CUtensorMap mX_K, mW_K, mG_st, mA4, mB4, mA5, mB5, mdW, mdX;
+      if ((rc = make_map(&mX_K, X, dt, elt, H, N, H * elt, KE, BM, "X (K-major)"))) return rc;
+      if ((rc = make_map(&mW_K, W, dt, elt, H, V, H * elt, KE, BN, "W (K-major)"))) return rc;
+      if ((rc = make_map(&mG_st, G, dt, elt, Vc, N, Vc * elt, KE, 32, "G store"))) return rc;
+      if ((rc = make_map(&mA5, G, dt, elt, Vc, N, Vc * elt, KE, BM, "G (K-major)"))) return rc;
+      if (bf16) {
+        if ((rc = make_map(&mA4, G, dt, elt, Vc, N, Vc * elt, KE, KE, "G (MN-major)")))
+          return rc;
+        if ((rc = make_map(&mB4, X, dt, elt, H, N, H * elt, KE, KE, "X (MN-major)"))) return rc;
+        if ((rc = make_map(&mB5, W, dt, elt, H, V, H * elt, KE, KE, "W (MN-major)"))) return rc;
+      } else {
+        if ((rc = make_map(&mA4, Gt, dt, 4, N, Vc, Np * 4, KE, BM, "G^T (K-major)"))) return rc;
+        if ((rc = make_map(&mB4, Xt, dt, 4, N, H, Np * 4, KE, BN, "X^T (K-major)"))) return rc;
+        if ((rc = make_map(&mB5, Wt, dt, 4, Vc, H, Vc * 4, KE, BN, "W^T chunk (K-major)")))
+          return rc;
+        FLCE_CUDA(launch_transpose_f32(static_cast<const float*>(X), N, H, H, Xt, Np, Np,
+                                       D.sms, s));
+      }
+      if ((rc = make_map(&mdW, dW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, V, H * 4, 32, 32,
+                         "dW store")))
+        return rc;
+      if ((rc = make_map(&mdX, dxacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, N, H * 4, 32, 32,
+                         "dX accumulator")))
+        return rc;
+      const int32_t m_tok = static_cast<int32_t>((N + BM - 1) / BM);
+      const int32_t n_h = static_cast<int32_t>((H + BN - 1) / BN);
+      for (int64_t c = 0; c < P.num_chunks; ++c) {
+        const int64_t c0 = c * Vc;
+        const int64_t vc = (V - c0) < Vc ? (V - c0) : Vc;
+        // pass 2: G_c
+        {
+          GemmGrid g{};
+          g.num_m_blk = m_tok;
+          g.num_n_blk = static_cast<int32_t>((vc + BN - 1) / BN);
+          g.num_k_blk = static_cast<int32_t>((H + KE - 1) / KE);
+          g.b_mn_off = static_cast<int32_t>(c0);
+          g.status = &sc->status;
+          GradLogitsParams gp{target, lse2, sc, N, V, ignore_index, c0};
+          const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, D.sms);
+          FLCE_CUDA(bf16 ? launch_logits_grad_bf16(mX_K, mW_K, mG_st, g, gp, grid, s)
+                         : launch_logits_grad_fp32(mX_K, mW_K, mG_st, g, gp, grid, s));
+          if ((rc = tr.after(FLCE_TRACE_LOGITS_GRAD))) return rc;
+        }
+        if (!bf16) {
+          FLCE_CUDA(launch_transpose_f32(reinterpret_cast<const float*>(G), N, Vc, Vc, Gt, Np,
+                                         Np, D.sms, s));
+          FLCE_CUDA(launch_transpose_f32(static_cast<const float*>(W) + c0 * H, vc, H, H, Wt,
+                                         Vc, Vc, D.sms, s));
+        }
+        // dW[c0 : c0+vc] = G_c^T X
+        {
+          GemmGrid g{};
+          g.num_m_blk = static_cast<int32_t>((vc + BM - 1) / BM);
+          g.num_n_blk = n_h;
+          g.num_k_blk = static_cast<int32_t>((N + KE - 1) / KE);
+          g.status = &sc->status;
+          StoreParams sp{0, static_cast<int32_t>(c0), 0};
+          const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, D.sms);
+          FLCE_CUDA(bf16 ? launch_dw_bf16(mA4, mB4, mdW, g, sp, grid, s)
+                         : launch_dw_fp32(mA4, mB4, mdW, g, sp, grid, s));
+          if ((rc = tr.after(FLCE_TRACE_DW))) return rc;
+        }
+        // dX_acc (+)= G_c W[c0 : c0+vc]
+        {
+          GemmGrid g{};
+          g.num_m_blk = m_tok;
+          g.num_n_blk = n_h;
+          g.num_k_blk = static_cast<int32_t>((vc + KE - 1) / KE);
+          g.b_k_off = bf16 ? static_cast<int32_t>(c0) : 0;
+          g.status = &sc->status;
+          StoreParams sp{0, 0, c > 0 ? 1 : 0};
+          const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, D.sms);
+          FLCE_CUDA(bf16 ? launch_dx_bf16(mA5, mB5, mdX, g, sp, grid, s)
+                         : launch_dx_fp32(mA5, mB5, mdX, g, sp, grid, s));
+          if ((rc = tr.after(FLCE_TRACE_DX))) return rc;
+        }
+      }
+      if (bf16) {
+        FLCE_CUDA(launch_convert_bf16(dxacc, dX, N * H, D.sms, s));
+        if ((rc = tr.after(FLCE_TRACE_CONVERT))) return rc;
+      }
+    }
+  }
+  if (o.status_dev) FLCE_CUDA(launch_status_code(sc, o.status_dev, s));
+  tr.finish();
+  return FLCE_OK;
+}
+
+int status_from_bits(int32_t bits) {
+  if (bits & FLCE_DEV_TIMEOUT) {
+    set_error("a bounded wait inside a kernel expired");
+    return FLCE_ERR_TIMEOUT;
+  }
+  if (bits & FLCE_DEV_TARGET) {
+    set_error("a target is outside [0, V) and is not the ignore index");
+    return FLCE_ERR_TARGET;
+  }
+  return FLCE_OK;
+}
+
+int entry(const void* X, const void* W, const int64_t* target, int64_t N, int64_t H, int64_t V,
+          int64_t ignore_index, float* loss_host, void* dX, float* dW, const flce_opts* opts_in,
+          bool grads) {
+  g_last_error[0] = 0;
+  flce_opts o;
+  flce_opts_init(&o);
+  if (opts_in) o = *opts_in;
+  int rc = check_args(X, W, target, N, H, V, o);
+  if (rc) return rc;
+  if (grads) {
+    if (!dW || (N > 0 && !dX)) {
+      set_error("null gradient pointer");
+      return FLCE_ERR_ARG;
+    }
+    if ((reinterpret_cast<uintptr_t>(dX) | reinterpret_cast<uintptr_t>(dW)) & 15u) {
+      set_error("dX and dW must be 16-byte aligned");
+      return FLCE_ERR_ALIGN;
+    }
+  }
+  const bool sync = o.sync != 0 || loss_host != nullptr;
+  DeviceInfo D;
+  if ((rc = device_info(o.dtype, &D))) return rc;
+
+  Plan P;
+  if ((rc = make_plan(&P, N, H, V, grads, o, o.workspace ? o.workspace_bytes : o.workspace_budget)))
+    return rc;
+  if (o.workspace && o.workspace_bytes < P.total) {
+    set_error("workspace of %zu bytes is smaller than the %zu bytes this call needs",
+              o.workspace_bytes, P.total);
+    return FLCE_ERR_WORKSPACE;
+  }
+  if (o.workspace && (reinterpret_cast<uintptr_t>(o.workspace) & 255u)) {
+    set_error("workspace must be 256-byte aligned");
+    return FLCE_ERR_ALIGN;
+  }
+  if (o.workspace_used) *o.workspace_used = P.total;
+  if (o.vocab_chunk_used) *o.vocab_chunk_used = P.Vc;
+
+  cudaStream_t s = static_cast<cudaStream_t>(o.stream);
+  uint8_t* ws = static_cast<uint8_t*>(o.workspace);
+  bool owned = false;
+  if (!ws) {
+    void* p = nullptr;
+    FLCE_CUDA(cudaMallocAsync(&p, P.total, s));
+    ws = static_cast<uint8_t*>(p);
+    owned = true;
+  }
+  rc = run_path(P, D, X, W, target, ignore_index, dX, dW, ws, o, s);
+  Scalars host_sc{};
+  if (rc == FLCE_OK && sync) {
+    cudaError_t e = cudaMemcpyAsync(&host_sc, ws + P.off_sc, sizeof(Scalars),
+                                    cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemcpyAsync(scalars)");
+  }
+  if (owned) {
+    cudaError_t e = cudaFreeAsync(ws, s);
+    if (e != cudaSuccess && rc == FLCE_OK) rc = cuda_fail(e, "cudaFreeAsync(workspace)");
+  }
+  if (rc != FLCE_OK) return rc;
+  if (sync) {
+    FLCE_CUDA(cudaStreamSynchronize(s));
+    if ((rc = status_from_bits(host_sc.status))) return rc;
+    if (loss_host) *loss_host = host_sc.loss;
+  }
+  return FLCE_OK;
+}
+
+}  // namespace
+}  // namespace flce
+
+using namespace flce;
+
+extern "C" {
+
+void flce_opts_init(flce_opts* o) {
+  if (!o) return;
+  std::memset(o, 0, sizeof *o);
+  o->dtype = FLCE_BF16;
+  o->sync = 1;
+  o->grad_scale = 1.0f;
+}
+
+int flce_fwd_bwd(const void* X, const void* W, const int64_t* target, int64_t N, int64_t H,
+                 int64_t V, int64_t ignore_index, float* loss, void* dX, float* dW) {
+  if (!loss) {
+    set_error("loss pointer is null");
+    return FLCE_ERR_ARG;
+  }
+  return entry(X, W, target, N, H, V, ignore_index, loss, dX, dW, nullptr, true);
+}
+
+int flce_fwd_bwd_ex(const void* X, const void* W, const int64_t* target, int64_t N, int64_t H,
+                    int64_t V, int64_t ignore_index, float* loss, void* dX, float* dW,
+                    const flce_opts* opts) {
+  return entry(X, W, target, N, H, V, ignore_index, loss, dX, dW, opts, true);
+}
+
+int flce_fwd(const void* X, const void* W, const int64_t* target, int64_t N, int64_t H, int64_t V,
+             int64_t ignore_index, float* loss, const flce_opts* opts) {
+  return entry(X, W, target, N, H, V, ignore_index, loss, nullptr, nullptr, opts, false);
+}
+
+int flce_fwd_bwd_host(const void* X_host, const void* W_host, const int64_t* target_host,
+                      int64_t N, int64_t H, int64_t V, int64_t ignore_index, float* loss,
+                      void* dX_host, float* dW_host, const flce_opts* opts_in) {
+  g_last_error[0] = 0;
+  flce_opts o;
+  flce_opts_init(&o);
+  if (opts_in) o = *opts_in;
+  if (!loss || !dW_host || !W_host || (N > 0 && (!X_host || !target_host || !dX_host))) {
+    set_error("null host pointer");
+    return FLCE_ERR_ARG;
+  }
+  if (N < 0 || H <= 0 || V <= 0) {
+    set_error("bad sizes");
+    return FLCE_ERR_ARG;
+  }
+  const size_t elt = (o.dtype == FLCE_FP32) ? 4 : 2;
+  const size_t bx = static_cast<size_t>(N) * H * elt, bw = static_cast<size_t>(V) * H * elt,
+               bt = static_cast<size_t>(N) * 8, bdw = static_cast<size_t>(V) * H * 4;
+  cudaStream_t s = static_cast<cudaStream_t>(o.stream);
+  const size_t ox = 0, ow = align_up(ox + bx, 256), ot = align_up(ow + bw, 256),
+               odx = align_up(ot + bt, 256), odw = align_up(odx + bx, 256),
+               total = align_up(odw + bdw, 256);
+  void* buf = nullptr;
+  FLCE_CUDA(cudaMallocAsync(&buf, total, s));
+  uint8_t* b = static_cast<uint8_t*>(buf);
+  int rc = FLCE_OK;
+  cudaError_t e = cudaSuccess;
+  if (bx) e = cudaMemcpyAsync(b + ox, X_host, bx, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(b + ow, W_host, bw, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && bt) e = cudaMemcpyAsync(b + ot, target_host, bt, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemcpyAsync(H2D)");
+  if (rc == FLCE_OK) {
+    o.sync = 1;
+    rc = entry(b + ox, b + ow, reinterpret_cast<const int64_t*>(b + ot), N, H, V, ignore_index,
+               loss, b + odx, reinterpret_cast<float*>(b + odw), &o, true);
+  }
+  if (rc == FLCE_OK) {
+    if (bx) e = cudaMemcpyAsync(dX_host, b + odx, bx, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dW_host, b + odw, bdw, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemcpyAsync(D2H)");
+  }
+  e = cudaFreeAsync(buf, s);
+  if (e != cudaSuccess && rc == FLCE_OK) rc = cuda_fail(e, "cudaFreeAsync");
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess && rc == FLCE_OK) rc = cuda_fail(e, "cudaStreamSynchronize");
+  return rc;
+}
+
+size_t flce_workspace_bytes(int64_t N, int64_t H, int64_t V, int with_grads,
+                            const flce_opts* opts_in) {
+  flce_opts o;
+  flce_opts_init(&o);
+  if (opts_in) o = *opts_in;
+  if (N < 0 || H <= 0 || V <= 0) return 0;
+  Plan P;
+  if (make_plan(&P, N, H, V, with_grads != 0, o, o.workspace_budget) != FLCE_OK) return 0;
+  return P.total;
+}
+
+const char* flce_status_str(int s) {
+  switch (s) {
+    case FLCE_OK: return "ok";
+    case FLCE_ERR_ARG: return "invalid argument";
+    case FLCE_ERR_ALIGN: return "misaligned pointer or row pitch";
+    case FLCE_ERR_ARCH: return "device is not compute capability 10.3";
+    case FLCE_ERR_TARGET: return "target outside [0, V) that is not the ignore index";
+    case FLCE_ERR_WORKSPACE: return "workspace too small";
+    case FLCE_ERR_CUDA: return "CUDA error";
+    case FLCE_ERR_TIMEOUT: return "bounded wait expired inside a kernel";
+    default: return "unknown status";
+  }
+}
+
+const char* flce_last_error(void) { return g_last_error; }
+
+int flce_version(void) { return FLCE_VERSION; }
+
+size_t flce_opts_sizeof(void) { return sizeof(flce_opts); }
+
+}  // extern "C"

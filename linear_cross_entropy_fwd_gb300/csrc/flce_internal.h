@@ -1,0 +1,52 @@
+// flce_internal.h -- definitions shared by the host code and the kernels of
+// libflce (not part of the public C ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+namespace flce {
+
+// Bits of the per-call device status word.
+enum : int32_t {
+  FLCE_DEV_TARGET = 1,   // a target outside [0, V) that is not the ignore index
+  FLCE_DEV_TIMEOUT = 2,  // a bounded wait inside a kernel expired
+};
+
+// GEMM tile: BM token/vocab rows x BN columns, K staged 128 bytes at a time.
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * 128;
+constexpr int B_STAGE_BYTES = BN * 128;
+constexpr int EPI_WARPS = 4;
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr int STAGING_BUF_BYTES = 4096;              // one 32-row x 128-byte TMA store box
+constexpr int STAGING_BYTES = EPI_WARPS * 2 * STAGING_BUF_BYTES;
+constexpr int TMEM_COLS = 2 * BN;                    // two fp32 accumulators of BN columns
+constexpr int SMEM_BARRIER_BYTES = 256;
+constexpr int GEMM_SMEM_BYTES =
+    1024 + STAGES * (A_STAGE_BYTES + B_STAGE_BYTES) + STAGING_BYTES + SMEM_BARRIER_BYTES;
+
+// Tile space and TMA coordinate offsets of one GEMM launch.
+struct GemmGrid {
+  int32_t num_m_blk;
+  int32_t num_n_blk;
+  int32_t num_k_blk;   // K blocks of 128 bytes
+  int32_t a_mn_off;    // element offsets added to operand coordinates
+  int32_t a_k_off;
+  int32_t b_mn_off;
+  int32_t b_k_off;
+  int32_t* status;     // device status word (FLCE_DEV_* bits)
+};
+
+// Small device-side scalars of one call.
+struct Scalars {
+  int32_t status;
+  uint32_t ticket;
+  int64_t n_valid;
+  float scale;        // grad_scale / normaliser (0 when nothing is valid)
+  float loss;
+  double loss_sum;
+};
+
+}  // namespace flce

@@ -1,0 +1,99 @@
+// launch.h -- host-side launchers of the libflce kernels (internal).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "flce_internal.h"
+
+namespace flce {
+
+struct RowLseParams {
+  const int64_t* target;
+  float* partial;
+  float* st;
+  int64_t N;
+  int64_t V;
+};
+
+struct GradLogitsParams {
+  const int64_t* target;
+  const float* lse2;
+  const Scalars* scalars;
+  int64_t N;
+  int64_t V;
+  int64_t ignore_index;
+  int64_t vocab_off;
+};
+
+struct StoreParams {
+  int32_t x_off;
+  int32_t y_off;
+  int32_t reduce;
+};
+
+// Set the dynamic shared-memory limit of every GEMM kernel on the current device.
+cudaError_t gemm_prepare_bf16();
+cudaError_t gemm_prepare_fp32();
+
+// Pass 1: A = X (K-major), B = W (K-major), epilogue = per-tile row statistics.
+cudaError_t launch_logits_lse_bf16(const CUtensorMap& A, const CUtensorMap& B, const GemmGrid& g,
+                                   const RowLseParams& p, int grid, cudaStream_t s);
+cudaError_t launch_logits_lse_fp32(const CUtensorMap& A, const CUtensorMap& B, const GemmGrid& g,
+                                   const RowLseParams& p, int grid, cudaStream_t s);
+// Pass 2: A = X (K-major), B = W chunk (K-major), epilogue = G chunk store.
+cudaError_t launch_logits_grad_bf16(const CUtensorMap& A, const CUtensorMap& B,
+                                    const CUtensorMap& out, const GemmGrid& g,
+                                    const GradLogitsParams& p, int grid, cudaStream_t s);
+cudaError_t launch_logits_grad_fp32(const CUtensorMap& A, const CUtensorMap& B,
+                                    const CUtensorMap& out, const GemmGrid& g,
+                                    const GradLogitsParams& p, int grid, cudaStream_t s);
+// dW chunk: A = G^T, B = X (bf16: both MN-major views of G and X; fp32:
+// K-major transposed copies G^T [Vc, N] and X^T [H, N]), fp32 store.
+cudaError_t launch_dw_bf16(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& out,
+                           const GemmGrid& g, const StoreParams& p, int grid, cudaStream_t s);
+cudaError_t launch_dw_fp32(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& out,
+                           const GemmGrid& g, const StoreParams& p, int grid, cudaStream_t s);
+// dX chunk: A = G (K-major), B = W chunk (bf16: MN-major view of W; fp32:
+// K-major transposed copy W_c^T [H, Vc]), fp32 store or add.
+cudaError_t launch_dx_bf16(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& out,
+                           const GemmGrid& g, const StoreParams& p, int grid, cudaStream_t s);
+cudaError_t launch_dx_fp32(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& out,
+                           const GemmGrid& g, const StoreParams& p, int grid, cudaStream_t s);
+
+// Row combine: partial statistics -> lse2, row losses, mean loss, n_valid, scale.
+struct CombineParams {
+  const float* partial;   // [num_vblk][N]
+  int32_t num_vblk;
+  const float* st;        // [N]
+  const int64_t* target;  // [N]
+  int64_t N;
+  int64_t V;
+  int64_t ignore_index;
+  float* lse2;            // [N] (workspace)
+  float* lse_out;         // optional [N]
+  float* loss_rows_out;   // optional [N]
+  double* blk_loss;       // [grid]
+  int64_t* blk_cnt;       // [grid]
+  Scalars* sc;
+  float grad_scale;
+  int64_t norm_count;
+  float* loss_out;        // optional device
+  int64_t* nvalid_out;    // optional device
+};
+constexpr int COMBINE_THREADS = 256;
+int combine_grid(int64_t N);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+
+// Device status bits -> flce_status code in *out (one thread).
+cudaError_t launch_status_code(const Scalars* sc, int32_t* out, cudaStream_t s);
+
+// out[c * out_pitch + r] = in[r * in_pitch + c] for r < R, c < C, and 0 for
+// R <= r < R_pad (fp32).
+cudaError_t launch_transpose_f32(const float* in, int64_t R, int64_t C, int64_t in_pitch,
+                                 float* out, int64_t out_pitch, int64_t R_pad, int sms,
+                                 cudaStream_t s);
+
+// fp32 [n] -> bf16 [n] (round to nearest even).
+cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t n, int sms, cudaStream_t s);
+
+}  // namespace flce

@@ -43,22 +43,35 @@
 
 enum { ORC_F64 = 0, ORC_F32 = 1, ORC_BF16 = 2 };
 
-static double elem(const void *p, int type, int64_t i) {
-  if (type == ORC_F64) return ((const double *)p)[i];
-  if (type == ORC_F32) return (double)((const float *)p)[i];
-  /* bfloat16: the upper 16 bits of an IEEE float32 */
-  uint32_t bits = (uint32_t)((const uint16_t *)p)[i] << 16;
+
+static double bf16_to_double(uint16_t v) {
+  uint32_t bits = (uint32_t)v << 16;
   float f;
   memcpy(&f, &bits, sizeof f);
   return (double)f;
 }
 
-/* S_ij = sum_h X[i,h] * W[j,h] */
+static double elem(const void *p, int type, int64_t i) {
+  if (type == ORC_F64) return ((const double *)p)[i];
+  if (type == ORC_F32) return (double)((const float *)p)[i];
+  /* bfloat16: the upper 16 bits of an IEEE float32 */
+  return bf16_to_double(((const uint16_t *)p)[i]);
+}
+
+/* S_ij = sum_h X[i,h] * W[j,h]  (one loop per element type; same order) */
 static double logit(const void *X, const void *W, int type, int64_t H,
                     int64_t i, int64_t j) {
   double s = 0.0;
-  for (int64_t h = 0; h < H; ++h)
-    s += elem(X, type, i * H + h) * elem(W, type, j * H + h);
+  if (type == ORC_F64) {
+    const double *x = (const double *)X + i * H, *w = (const double *)W + j * H;
+    for (int64_t h = 0; h < H; ++h) s += x[h] * w[h];
+  } else if (type == ORC_F32) {
+    const float *x = (const float *)X + i * H, *w = (const float *)W + j * H;
+    for (int64_t h = 0; h < H; ++h) s += (double)x[h] * (double)w[h];
+  } else {
+    const uint16_t *x = (const uint16_t *)X + i * H, *w = (const uint16_t *)W + j * H;
+    for (int64_t h = 0; h < H; ++h) s += bf16_to_double(x[h]) * bf16_to_double(w[h]);
+  }
   return s;
 }
 

@@ -1,0 +1,84 @@
+"""CPU-only checks of the boundary: the library builds for sm_103a, loads
+without a GPU, exports every symbol include/flce.h declares, agrees with the
+binding on the options layout, and plans workspaces as documented."""
+import os
+import re
+
+import pytest
+
+import linear_cross_entropy_fwd_gb300 as flce
+from linear_cross_entropy_fwd_gb300 import build as flce_build
+from flce_synth import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    flce_build.build()
+    return flce.load_library()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "flce.h")).read()
+    return re.findall(r"FLCE_API\s+[\w\s\*]+?\b(flce_\w+)\s*\(", src)
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for must in ["flce_fwd_bwd", "flce_fwd_bwd_ex", "flce_fwd", "flce_fwd_bwd_host",
+                 "flce_workspace_bytes", "flce_status_str", "flce_last_error",
+                 "flce_opts_init"]:
+        assert must in names
+    assert sorted(names) == sorted(flce.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_opts_layout_and_version(lib):
+    import ctypes
+    assert lib.flce_opts_sizeof() == ctypes.sizeof(flce.FlceOpts)
+    assert lib.flce_version() == 1
+    o = flce.make_opts()
+    assert o.sync == 1 and o.grad_scale == 1.0 and o.dtype == flce.FLCE_BF16
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.flce_status_str(s)
+    assert lib.flce_status_str(999) == b"unknown status"
+
+
+def test_workspace_plans(lib):
+    # loss only: no gradient chunk, no dX accumulator
+    w = WORKLOADS["llama3_8b_head_8192x4096x128256"]
+    fwd = flce.flce_workspace_bytes(w.N, w.H, w.V, with_grads=False)
+    assert fwd < 20 * 2 ** 20
+    for name in ["llama3_8b_head_8192x4096x128256", "long_context_65536x4096x128256",
+                 "qwen2_7b_head_16384x3584x152064"]:
+        w = WORKLOADS[name]
+        ws = flce.flce_workspace_bytes(w.N, w.H, w.V)
+        assert 0 < ws <= w.N * w.V * 4 // 16, name
+    # an explicit chunk width is honoured; a smaller budget gives a smaller plan
+    a = flce.flce_workspace_bytes(8192, 4096, 128256, vocab_chunk=1024)
+    b = flce.flce_workspace_bytes(8192, 4096, 128256, vocab_chunk=2048)
+    assert b - a == 8192 * 1024 * 2
+    small = flce.flce_workspace_bytes(8192, 4096, 128256, workspace_budget=150 * 2 ** 20)
+    assert small <= 150 * 2 ** 20 + 8192 * 256 * 2
+    # bad sizes plan nothing
+    assert flce.flce_workspace_bytes(10, 0, 5) == 0
+    assert flce.flce_workspace_bytes(10, 8, 5, vocab_chunk=300) == 0
+
+
+def test_product_path_has_no_oracle_import():
+    """The CUDA package never reaches into the oracle or the generator."""
+    pkg = os.path.join(ROOT, "linear_cross_entropy_fwd_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in src.replace("oracle/", ""), f
+                assert "flce_synth" not in src, f

@@ -1,0 +1,237 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle,
+element by element, at sizes the oracle finishes in seconds; plus the edge
+cases (ragged tiles, targets in the last partial vocabulary tile, all rows
+ignored, N = 0, bad targets) and the error paths of the boundary."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from flce_synth import make_case
+from parity_util import assert_grad, assert_loss
+
+pytestmark = pytest.mark.gpu
+IGN = -100
+DEV = "cuda"
+
+
+def _gpu(X, W, t):
+    return X.to(DEV), W.to(DEV), t.to(DEV)
+
+
+def _check_full(flce, X, W, t, vocab_chunk=0, ignore_index=IGN):
+    Xd, Wd, td = _gpu(X, W, t)
+    N = X.shape[0]
+    lse = torch.empty(N, device=DEV)
+    rows = torch.empty(N, device=DEV)
+    info = {}
+    loss, nval, dX, dW = flce.flce_fwd_bwd_ex(Xd, Wd, td, ignore_index, sync=True,
+                                              lse_out=lse, loss_rows_out=rows,
+                                              vocab_chunk=vocab_chunk, info=info)
+    ref = oracle.flce(X, W, t, ignore_index)
+    assert int(nval.item()) == ref["n_valid"]
+    assert_loss(loss.item(), ref["loss"])
+    if N:
+        assert_loss(lse.cpu().numpy(), ref["lse"], "lse")
+        assert_loss(rows.cpu().numpy(), ref["loss_rows"], "row loss")
+        assert_grad(dX.float().cpu().numpy(), ref["dX"], "dX")
+    assert_grad(dW.cpu().numpy(), ref["dW"], "dW")
+    assert int(info["status"].item()) == 0
+    return info
+
+
+CASES = [
+    # N, H, V, dtype, ignored %, vocab_chunk
+    (4, 128, 256, "fp32", 0, 0),        # the overview's worked-example shape
+    (1, 64, 256, "bf16", 0, 0),         # one row
+    (127, 64, 255, "bf16", 10, 0),      # all ragged, V below one vocabulary tile
+    (300, 192, 1000, "bf16", 10, 0),    # ragged M, K, V tails
+    (513, 320, 3000, "bf16", 5, 512),   # six chunks, ragged last chunk
+    (700, 320, 3000, "fp32", 10, 512),  # tf32 path with chunks
+    (256, 4096, 2048, "bf16", 2, 0),    # long K (64 stages of the ring)
+    (2050, 136, 777, "bf16", 30, 256),  # 17 row tiles, K tail of 8, 4 chunks
+    (389, 100, 1300, "fp32", 20, 768),  # fp32 with odd N (transpose padding)
+]
+
+
+@pytest.mark.parametrize("N,H,V,dtype,ign,vc", CASES)
+def test_fwd_bwd_matches_oracle(cuda_lib, N, H, V, dtype, ign, vc):
+    X, W, t = make_case(N, H, V, dtype, seed=N + V, ignore_num=ign,
+                        w_std=0.088 if dtype == "fp32" else 0.02)
+    info = _check_full(cuda_lib, X, W, t, vocab_chunk=vc)
+    if vc:
+        assert info["vocab_chunk"] == vc
+
+
+def test_large_logits_range(cuda_lib):
+    """W scaled up so logits span about +-40: the max-shifted sums must hold."""
+    X, W, t = make_case(200, 256, 1500, "bf16", seed=9, ignore_num=5, w_std=0.15)
+    _check_full(cuda_lib, X, W, t)
+
+
+def test_targets_in_last_partial_tile(cuda_lib):
+    X, W, _ = make_case(130, 64, 700, "bf16", seed=11)
+    t = torch.arange(130, dtype=torch.int64) % 188 + 512  # every target in [512, 700)
+    t[5] = IGN
+    _check_full(cuda_lib, X, W, t)
+    t2 = torch.full((130,), 699, dtype=torch.int64)     # the very last column
+    _check_full(cuda_lib, X, W, t2, vocab_chunk=256)
+
+
+def test_all_ignored_gives_zero(cuda_lib):
+    X, W, _ = make_case(64, 64, 512, "bf16", seed=12)
+    t = torch.full((64,), IGN, dtype=torch.int64)
+    loss, nval, dX, dW = cuda_lib.flce_fwd_bwd_ex(*_gpu(X, W, t), IGN, sync=True)
+    assert loss.item() == 0.0 and nval.item() == 0
+    assert dX.abs().max().item() == 0.0 and dW.abs().max().item() == 0.0
+
+
+def test_single_valid_row(cuda_lib):
+    X, W, _ = make_case(96, 64, 512, "bf16", seed=13)
+    t = torch.full((96,), IGN, dtype=torch.int64)
+    t[77] = 3
+    _check_full(cuda_lib, X, W, t)
+
+
+def test_empty_batch(cuda_lib):
+    X = torch.zeros((0, 64), dtype=torch.bfloat16, device=DEV)
+    W = torch.randn(300, 64, device=DEV).to(torch.bfloat16)
+    t = torch.zeros((0,), dtype=torch.int64, device=DEV)
+    dW = torch.full((300, 64), 7.0, device=DEV)
+    loss, nval, dX, dW = cuda_lib.flce_fwd_bwd_ex(X, W, t, IGN, sync=True, dW=dW)
+    assert loss.item() == 0.0 and nval.item() == 0
+    assert dW.abs().max().item() == 0.0
+
+
+def test_custom_ignore_index(cuda_lib):
+    X, W, t = make_case(150, 64, 600, "bf16", seed=14, ignore_num=20, ignore_index=0)
+    _check_full(cuda_lib, X, W, t, ignore_index=0)
+
+
+def test_bad_target_reports_error(cuda_lib):
+    X, W, _ = make_case(40, 64, 300, "bf16", seed=15)
+    for bad in (300, -1, 10 ** 9):
+        t = torch.zeros(40, dtype=torch.int64)
+        t[17] = bad
+        with pytest.raises(cuda_lib.FlceError) as ei:
+            cuda_lib.flce_fwd_bwd_ex(*_gpu(X, W, t), IGN, sync=True)
+        assert ei.value.status == cuda_lib.FLCE_ERR_TARGET
+    # asynchronous form: the status lands in the device word
+    t = torch.zeros(40, dtype=torch.int64)
+    t[0] = 300
+    info = {}
+    cuda_lib.flce_fwd_bwd_ex(*_gpu(X, W, t), IGN, sync=False, info=info)
+    torch.cuda.synchronize()
+    assert int(info["status"].item()) == cuda_lib.FLCE_ERR_TARGET
+    # a good call afterwards is unaffected
+    t[0] = 5
+    _check_full(cuda_lib, X, W, t)
+
+
+def test_loss_only_entry(cuda_lib):
+    X, W, t = make_case(333, 128, 1234, "bf16", seed=16, ignore_num=15)
+    Xd, Wd, td = _gpu(X, W, t)
+    lse = torch.empty(333, device=DEV)
+    rows = torch.empty(333, device=DEV)
+    info = {}
+    loss, nval = cuda_lib.flce_fwd(Xd, Wd, td, IGN, sync=True, lse_out=lse,
+                                   loss_rows_out=rows, info=info)
+    ref = oracle.flce(X, W, t, IGN, grads=False)
+    assert nval.item() == ref["n_valid"]
+    assert_loss(loss.item(), ref["loss"])
+    assert_loss(lse.cpu().numpy(), ref["lse"], "lse")
+    assert_loss(rows.cpu().numpy(), ref["loss_rows"], "row loss")
+    # the loss-only plan holds no gradient chunk
+    assert info["workspace_bytes"] < cuda_lib.flce_workspace_bytes(333, 128, 1234, True)
+
+
+def test_simple_and_host_entry_points(cuda_lib):
+    X, W, t = make_case(257, 64, 900, "bf16", seed=17, ignore_num=10)
+    ref = oracle.flce(X, W, t, IGN)
+    loss, dX, dW = cuda_lib.flce_fwd_bwd(*_gpu(X, W, t), IGN)
+    assert_loss(loss, ref["loss"])
+    assert_grad(dX.float().cpu().numpy(), ref["dX"], "dX")
+    assert_grad(dW.cpu().numpy(), ref["dW"], "dW")
+    loss_h, dX_h, dW_h = cuda_lib.flce_fwd_bwd_host(X.pin_memory(), W.pin_memory(),
+                                                    t.pin_memory(), IGN)
+    assert loss_h == loss
+    assert torch.equal(dX_h, dX.cpu()) and torch.equal(dW_h, dW.cpu())
+
+
+def test_deterministic(cuda_lib):
+    X, W, t = make_case(600, 256, 4000, "bf16", seed=18, ignore_num=5)
+    Xd, Wd, td = _gpu(X, W, t)
+    a = cuda_lib.flce_fwd_bwd_ex(Xd, Wd, td, IGN, sync=True, vocab_chunk=1024)
+    b = cuda_lib.flce_fwd_bwd_ex(Xd, Wd, td, IGN, sync=True, vocab_chunk=1024)
+    assert a[0].item() == b[0].item()
+    assert torch.equal(a[2], b[2]) and torch.equal(a[3], b[3])
+
+
+def test_grad_scale_and_norm_count(cuda_lib):
+    X, W, t = make_case(300, 128, 800, "bf16", seed=19, ignore_num=10)
+    Xd, Wd, td = _gpu(X, W, t)
+    base = cuda_lib.flce_fwd_bwd_ex(Xd, Wd, td, IGN, sync=True)
+    sc = cuda_lib.flce_fwd_bwd_ex(Xd, Wd, td, IGN, sync=True, grad_scale=0.25)
+    assert sc[0].item() == base[0].item()
+    torch.testing.assert_close(sc[3], base[3] * 0.25, rtol=1e-2, atol=1e-7)
+    n = int(base[1].item())
+    nc = cuda_lib.flce_fwd_bwd_ex(Xd, Wd, td, IGN, sync=True, norm_count=2 * n)
+    assert abs(nc[0].item() - base[0].item() / 2) <= 1e-6 * base[0].item()
+    torch.testing.assert_close(nc[3], base[3] * 0.5, rtol=1e-2, atol=1e-7)
+
+
+def test_autograd_module(cuda_lib):
+    X, W, t = make_case(200, 128, 700, "bf16", seed=20, ignore_num=10)
+    ref = oracle.flce(X, W, t, IGN)
+    w = W.to(DEV).requires_grad_(True)
+    x = X.to(DEV).requires_grad_(True)
+    loss = cuda_lib.LinearCrossEntropyLoss(IGN)(w, x, t.to(DEV))
+    (3.0 * loss).backward()
+    assert_loss(loss.item(), ref["loss"])
+    assert_grad(x.grad.float().cpu().numpy(), 3.0 * ref["dX"], "3 dX")
+    assert_grad(w.grad.float().cpu().numpy(), 3.0 * ref["dW"], "3 dW")
+
+
+def test_caller_workspace(cuda_lib):
+    X, W, t = make_case(300, 128, 2000, "bf16", seed=21, ignore_num=10)
+    need = cuda_lib.flce_workspace_bytes(300, 128, 2000, True, vocab_chunk=512)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    ref = oracle.flce(X, W, t, IGN)
+    Xd, Wd, td = _gpu(X, W, t)
+    loss, _, dX, dW = cuda_lib.flce_fwd_bwd_ex(Xd, Wd, td, IGN, sync=True, workspace=ws,
+                                               vocab_chunk=512)
+    assert_loss(loss.item(), ref["loss"])
+    assert_grad(dW.cpu().numpy(), ref["dW"], "dW")
+    with pytest.raises(cuda_lib.FlceError) as ei:
+        cuda_lib.flce_fwd_bwd_ex(Xd, Wd, td, IGN, sync=True, workspace=ws[:need // 2],
+                                 vocab_chunk=512)
+    assert ei.value.status == cuda_lib.FLCE_ERR_WORKSPACE
+
+
+def test_argument_errors(cuda_lib):
+    lib = cuda_lib.load_library()
+    X, W, t = _gpu(*make_case(16, 64, 256, "bf16", seed=22))
+    dX = torch.empty_like(X)
+    dW = torch.empty(256, 64, device=DEV)
+    loss = ctypes.c_float()
+    call = lambda *a: lib.flce_fwd_bwd(*a)  # noqa: E731
+    assert call(None, W.data_ptr(), t.data_ptr(), 16, 64, 256, IGN, ctypes.byref(loss),
+                dX.data_ptr(), dW.data_ptr()) == cuda_lib.FLCE_ERR_ARG
+    assert call(X.data_ptr(), W.data_ptr(), t.data_ptr(), 16, 64, 0, IGN, ctypes.byref(loss),
+                dX.data_ptr(), dW.data_ptr()) == cuda_lib.FLCE_ERR_ARG
+    assert call(X.data_ptr(), W.data_ptr(), t.data_ptr(), 16, 64, 256, IGN, None,
+                dX.data_ptr(), dW.data_ptr()) == cuda_lib.FLCE_ERR_ARG
+    # H * 2 bytes = 24 is not a multiple of 16
+    X12 = torch.zeros(16, 12, dtype=torch.bfloat16, device=DEV)
+    W12 = torch.zeros(256, 12, dtype=torch.bfloat16, device=DEV)
+    assert call(X12.data_ptr(), W12.data_ptr(), t.data_ptr(), 16, 12, 256, IGN,
+                ctypes.byref(loss), dX.data_ptr(), dW.data_ptr()) == cuda_lib.FLCE_ERR_ALIGN
+    # misaligned X pointer
+    assert call(X.data_ptr() + 2, W.data_ptr(), t.data_ptr(), 15, 64, 256, IGN,
+                ctypes.byref(loss), dX.data_ptr(), dW.data_ptr()) == cuda_lib.FLCE_ERR_ALIGN
+    with pytest.raises(cuda_lib.FlceError) as ei:
+        cuda_lib.flce_fwd_bwd_ex(X, W, t, IGN, sync=True, vocab_chunk=300)
+    assert ei.value.status == cuda_lib.FLCE_ERR_ARG
+    assert lib.flce_last_error()  # a message was left for the caller

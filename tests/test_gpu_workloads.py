@@ -1,0 +1,134 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+benchmark times (default planner, default stream, bf16).
+
+The oracle cannot afford N x V x H at these sizes, so:
+  * sampled token rows: lse, row loss and the dX row against the oracle
+    computed row by row (n_valid counted over the full batch);
+  * dW and the loss: a prefix problem (the first tokens of the same
+    workload, same H and V, same launch configuration) compared with the
+    oracle in full, plus properties that hold at any size on the full run
+    (sum_j dW_j = 0, the loss equals the mean of its row losses, linearity of
+    dW over a split of the batch, bitwise determinism);
+  * n_valid bit-exact against N - floor(p N).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from flce_synth import WORKLOADS, make_inputs
+from parity_util import assert_grad, assert_loss
+
+pytestmark = pytest.mark.gpu
+IGN = -100
+DEV = "cuda"
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")))
+BIG = ["small_head_2048x2048x32000", "llama3_8b_head_8192x4096x128256",
+       "qwen2_7b_head_16384x3584x152064", "long_context_65536x4096x128256"]
+
+
+def _sample_rows(t: torch.Tensor, k: int = 10, seed: int = 0):
+    N = t.shape[0]
+    rng = np.random.default_rng(seed)
+    rows = {0, 1, N - 1, N // 2}
+    ign = torch.nonzero(t == IGN).flatten().tolist()
+    if ign:
+        rows.add(ign[0])
+    rows.update(rng.choice(N, size=k, replace=False).tolist())
+    return sorted(rows)
+
+
+@pytest.fixture(scope="module")
+def workload_cache():
+    return {}
+
+
+def _inputs(cache, name):
+    if name not in cache:
+        cache.clear()  # keep one workload resident at a time
+        cache[name] = make_inputs(WORKLOADS[name])
+    return cache[name]
+
+
+@pytest.mark.parametrize("name", BIG)
+def test_workload_sampled_rows(cuda_lib, workload_cache, name):
+    w = WORKLOADS[name]
+    X, W, t = _inputs(workload_cache, name)
+    Xd, Wd, td = X.to(DEV), W.to(DEV), t.to(DEV)
+    lse = torch.empty(w.N, device=DEV)
+    rows_out = torch.empty(w.N, device=DEV)
+    info = {}
+    loss, nval, dX, dW = cuda_lib.flce_fwd_bwd_ex(Xd, Wd, td, IGN, sync=True, lse_out=lse,
+                                                  loss_rows_out=rows_out, info=info)
+    n = int(nval.item())
+    assert n == GOLDEN["ignored_counts"][name]
+    rows = _sample_rows(t, seed=w.seed)
+    ref = oracle.flce_rows(X, W, t, rows, IGN)
+    assert ref["n_valid"] == n
+    assert_loss(lse[rows].cpu().numpy(), ref["lse"], "lse rows")
+    assert_loss(rows_out[rows].cpu().numpy(), ref["loss_rows"], "row losses")
+    assert_grad(dX[rows].float().cpu().numpy(), ref["dX"], "dX rows")
+    # properties of the full run
+    rl = rows_out.double()
+    assert abs(loss.item() - (rl.sum().item() / n)) <= 1e-5 * loss.item()
+    col_sum = dW.double().sum(dim=0).abs()
+    col_abs = dW.double().abs().sum(dim=0)
+    assert (col_sum <= 1e-2 * col_abs + 1e-12).all(), "sum_j dW_j is not ~0"
+    assert torch.isfinite(dX.float()).all() and torch.isfinite(dW).all()
+    # workspace bound: one sixteenth of the N x V fp32 logits where the fp32
+    # dX accumulator itself fits under it
+    bound = w.N * w.V * 4 // 16
+    if w.N * w.H * 4 < bound // 2:
+        assert info["workspace_bytes"] <= bound
+
+
+@pytest.mark.parametrize("name", BIG)
+def test_workload_prefix_full(cuda_lib, workload_cache, name):
+    """The first 64 tokens of the workload as a problem of its own: loss, lse,
+    dX in full and 24 sampled dW rows (targets, edges, random) vs the oracle."""
+    w = WORKLOADS[name]
+    X, W, t = _inputs(workload_cache, name)
+    Np = 64
+    Xp, tp = X[:Np].contiguous(), t[:Np].contiguous()
+    lse = torch.empty(Np, device=DEV)
+    loss, nval, dX, dW = cuda_lib.flce_fwd_bwd_ex(Xp.to(DEV), W.to(DEV), tp.to(DEV), IGN,
+                                                  sync=True, lse_out=lse)
+    ref = oracle.flce_rows(Xp, W, tp, list(range(Np)), IGN)
+    assert int(nval.item()) == ref["n_valid"]
+    valid = (tp != IGN).numpy()
+    assert_loss(loss.item(), ref["loss_rows"][valid].sum() / ref["n_valid"])
+    assert_loss(lse.cpu().numpy(), ref["lse"], "lse")
+    assert_grad(dX.float().cpu().numpy(), ref["dX"], "dX")
+    rng = np.random.default_rng(w.seed)
+    tv = tp[tp != IGN].tolist()
+    vocab = sorted(set(tv[:8]) | {0, w.V - 1, w.V // 2} |
+                   set(rng.choice(w.V, 13, replace=False).tolist()))
+    ref_dw = oracle.flce_dw_rows(Xp, W, tp, vocab, IGN)
+    assert_grad(dW[vocab].cpu().numpy(), ref_dw, "dW rows")
+
+
+def test_llama3_linearity_and_determinism(cuda_lib, workload_cache):
+    """dW of the full batch equals the count-weighted dW of its two halves,
+    and two runs of the full workload are bitwise identical."""
+    name = "llama3_8b_head_8192x4096x128256"
+    X, W, t = _inputs(workload_cache, name)
+    Xd, Wd, td = X.to(DEV), W.to(DEV), t.to(DEV)
+    full = cuda_lib.flce_fwd_bwd_ex(Xd, Wd, td, IGN, sync=True)
+    again = cuda_lib.flce_fwd_bwd_ex(Xd, Wd, td, IGN, sync=True)
+    assert full[0].item() == again[0].item()
+    assert torch.equal(full[2], again[2]) and torch.equal(full[3], again[3])
+    h = X.shape[0] // 2
+    a = cuda_lib.flce_fwd_bwd_ex(Xd[:h].contiguous(), Wd, td[:h].contiguous(), IGN, sync=True)
+    b = cuda_lib.flce_fwd_bwd_ex(Xd[h:].contiguous(), Wd, td[h:].contiguous(), IGN, sync=True)
+    nf, na, nb = (int(v[1].item()) for v in (full, a, b))
+    assert nf == na + nb
+    comb = (na * a[3].double() + nb * b[3].double()) / nf
+    assert_grad(full[3].double().cpu().numpy(), comb.cpu().numpy(), "dW split")
+    lc = (na * a[0].item() + nb * b[0].item()) / nf
+    assert abs(full[0].item() - lc) <= 1e-5 * lc
+    # dX rows of each half, rescaled to the full normaliser
+    assert_grad(full[2][:h].float().cpu().numpy(),
+                (a[2].float() * na / nf).cpu().numpy(), "dX first half")
