@@ -210,14 +210,24 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="flce", choices=["flce", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--shape", default=None,
+                    help="N,H,V: a synthetic case of that size with the workload's recipe "
+                         "(profiling runs; not a bench line)")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--vocab-chunk", type=int, default=0,
+                    help="chunk width override (0 = the library's planner)")
     ap.add_argument("--ref-tokens", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
 
+    from dataclasses import replace
+
     from flce_synth import WORKLOADS
     workload = WORKLOADS[args.workload]
+    if args.shape:
+        n_, h_, v_ = (int(x) for x in args.shape.split(","))
+        workload = replace(workload, name=f"custom_{n_}x{h_}x{v_}", N=n_, H=h_, V=v_)
     if args.impl == "reference":
         return run_reference(args, workload)
 
@@ -245,7 +255,7 @@ def main():
 
     def step(trace=None, info=None):
         return flce.flce_fwd_bwd_ex(Xd, Wd, td, w.ignore_index, dX=dX, dW=dW, trace=trace,
-                                    info=info)
+                                    info=info, vocab_chunk=args.vocab_chunk)
 
     info = {}
     step(info=info)  # plans the call (chunk width) before the warm-up proper

@@ -53,8 +53,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct DeviceInfo {
   int sms = 0;
   bool ok_arch = false;
-  bool prepared_bf16 = false;
-  bool prepared_fp32 = false;
+  int units_bf16 = 0;  // resident CTA pairs of the bf16 GEMM kernels (0 = not prepared)
+  int units_fp32 = 0;  // resident CTAs of the fp32 GEMM kernels (0 = not prepared)
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
@@ -82,14 +82,8 @@ int device_info(int dtype, DeviceInfo* out) {
     }
   }
   if (!d.ok_arch) return FLCE_ERR_ARCH;
-  if (dtype == FLCE_BF16 && !d.prepared_bf16) {
-    FLCE_CUDA(gemm_prepare_bf16());
-    d.prepared_bf16 = true;
-  }
-  if (dtype == FLCE_FP32 && !d.prepared_fp32) {
-    FLCE_CUDA(gemm_prepare_fp32());
-    d.prepared_fp32 = true;
-  }
+  if (dtype == FLCE_BF16 && d.units_bf16 == 0) FLCE_CUDA(gemm_prepare_bf16(d.sms, &d.units_bf16));
+  if (dtype == FLCE_FP32 && d.units_fp32 == 0) FLCE_CUDA(gemm_prepare_fp32(d.sms, &d.units_fp32));
   *out = d;
   return FLCE_OK;
 }
@@ -183,6 +177,8 @@ size_t fixed_bytes(Plan& p) {
   return o;
 }
 
+constexpr int64_t kMinChunk = 2048;
+
 // budget: bytes the plan may use (0 = N*V*4/16).  Returns FLCE_OK or an error.
 int make_plan(Plan* out, int64_t N, int64_t H, int64_t V, bool grads, const flce_opts& o,
               size_t budget) {
@@ -213,7 +209,10 @@ int make_plan(Plan* out, int64_t N, int64_t H, int64_t V, bool grads, const flce
         per_col += static_cast<size_t>(p.Np) * 4 + static_cast<size_t>(H) * 4;
       const size_t avail = budget > fixed ? budget - fixed : 0;
       Vc = static_cast<int64_t>(avail / per_col) / BN * BN;
-      if (Vc < BN) Vc = BN;
+      // Narrower chunks cost more than they save: below kMinChunk columns the
+      // dW GEMM has too few tiles to fill the GPU, so the budget is exceeded
+      // rather than going below it.
+      if (Vc < kMinChunk) Vc = kMinChunk;
     }
     if (Vc > vpad) Vc = vpad;
     p.Vc = Vc;
@@ -307,6 +306,9 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
   const CUtensorMapDataType dt =
       bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const int KE = 128 / elt;  // K elements per 128-byte stage
+  const int64_t MB = bf16 ? 2 * BM : BM;  // rows of one tile (bf16: a CTA pair)
+  const uint32_t BR = bf16 ? BN / 2 : BN;  // rows of B one CTA stages (K-major box height)
+  const int units = bf16 ? D.units_bf16 : D.units_fp32;
   Scalars* sc = reinterpret_cast<Scalars*>(ws + P.off_sc);
   float* lse2 = reinterpret_cast<float*>(ws + P.off_lse2);
   float* st = reinterpret_cast<float*>(ws + P.off_st);
@@ -321,14 +323,14 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
   if (N > 0) {
     CUtensorMap mX, mW;
     if ((rc = make_map(&mX, X, dt, elt, H, N, H * elt, KE, BM, "X (K-major)"))) return rc;
-    if ((rc = make_map(&mW, W, dt, elt, H, V, H * elt, KE, BN, "W (K-major)"))) return rc;
+    if ((rc = make_map(&mW, W, dt, elt, H, V, H * elt, KE, BR, "W (K-major)"))) return rc;
     GemmGrid g{};
-    g.num_m_blk = static_cast<int32_t>((N + BM - 1) / BM);
+    g.num_m_blk = static_cast<int32_t>((N + MB - 1) / MB);
     g.num_n_blk = static_cast<int32_t>(P.num_vblk);
     g.num_k_blk = static_cast<int32_t>((H + KE - 1) / KE);
     g.status = &sc->status;
     RowLseParams rp{target, partial, st, N, V};
-    const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, D.sms);
+    const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, units);
     FLCE_CUDA(bf16 ? launch_logits_lse_bf16(mX, mW, g, rp, grid, s)
                    : launch_logits_lse_fp32(mX, mW, g, rp, grid, s));
     if ((rc = tr.after(FLCE_TRACE_LOGITS_LSE))) return rc;
@@ -368,7 +370,7 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
       // A/B maps of the dW GEMM (mA4, mB4) and of the dX GEMM (mA5, mB5)
       CUtensorMap mX_K, mW_K, mG_st, mA4, mB4, mA5, mB5, mdW, mdX;
       if ((rc = make_map(&mX_K, X, dt, elt, H, N, H * elt, KE, BM, "X (K-major)"))) return rc;
-      if ((rc = make_map(&mW_K, W, dt, elt, H, V, H * elt, KE, BN, "W (K-major)"))) return rc;
+      if ((rc = make_map(&mW_K, W, dt, elt, H, V, H * elt, KE, BR, "W (K-major)"))) return rc;
       if ((rc = make_map(&mG_st, G, dt, elt, Vc, N, Vc * elt, KE, 32, "G store"))) return rc;
       if ((rc = make_map(&mA5, G, dt, elt, Vc, N, Vc * elt, KE, BM, "G (K-major)"))) return rc;
       if (bf16) {
@@ -390,7 +392,7 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
       if ((rc = make_map(&mdX, dxacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, N, H * 4, 32, 32,
                          "dX accumulator")))
         return rc;
-      const int32_t m_tok = static_cast<int32_t>((N + BM - 1) / BM);
+      const int32_t m_tok = static_cast<int32_t>((N + MB - 1) / MB);
       const int32_t n_h = static_cast<int32_t>((H + BN - 1) / BN);
       for (int64_t c = 0; c < P.num_chunks; ++c) {
         const int64_t c0 = c * Vc;
@@ -404,7 +406,7 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
           g.b_mn_off = static_cast<int32_t>(c0);
           g.status = &sc->status;
           GradLogitsParams gp{target, lse2, sc, N, V, ignore_index, c0};
-          const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, D.sms);
+          const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, units);
           FLCE_CUDA(bf16 ? launch_logits_grad_bf16(mX_K, mW_K, mG_st, g, gp, grid, s)
                          : launch_logits_grad_fp32(mX_K, mW_K, mG_st, g, gp, grid, s));
           if ((rc = tr.after(FLCE_TRACE_LOGITS_GRAD))) return rc;
@@ -418,12 +420,13 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
         // dW[c0 : c0+vc] = G_c^T X
         {
           GemmGrid g{};
-          g.num_m_blk = static_cast<int32_t>((vc + BM - 1) / BM);
+          g.num_m_blk = static_cast<int32_t>((vc + MB - 1) / MB);
           g.num_n_blk = n_h;
           g.num_k_blk = static_cast<int32_t>((N + KE - 1) / KE);
           g.status = &sc->status;
+          g.raster_n = 1;  // a slab of G_c rows with all of X stays in L2
           StoreParams sp{0, static_cast<int32_t>(c0), 0};
-          const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, D.sms);
+          const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, units);
           FLCE_CUDA(bf16 ? launch_dw_bf16(mA4, mB4, mdW, g, sp, grid, s)
                          : launch_dw_fp32(mA4, mB4, mdW, g, sp, grid, s));
           if ((rc = tr.after(FLCE_TRACE_DW))) return rc;
@@ -435,9 +438,10 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
           g.num_n_blk = n_h;
           g.num_k_blk = static_cast<int32_t>((vc + KE - 1) / KE);
           g.b_k_off = bf16 ? static_cast<int32_t>(c0) : 0;
+          g.raster_n = 1;  // a slab of G_c rows with all of W[c] stays in L2
           g.status = &sc->status;
           StoreParams sp{0, 0, c > 0 ? 1 : 0};
-          const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, D.sms);
+          const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, units);
           FLCE_CUDA(bf16 ? launch_dx_bf16(mA5, mB5, mdX, g, sp, grid, s)
                          : launch_dx_fp32(mA5, mB5, mdX, g, sp, grid, s));
           if ((rc = tr.after(FLCE_TRACE_DX))) return rc;

@@ -36,8 +36,25 @@ struct GemmGrid {
   int32_t a_k_off;
   int32_t b_mn_off;
   int32_t b_k_off;
+  int32_t raster_n;    // 0: M index fastest in the tile order, 1: N index fastest
+  int32_t a_l2;        // L2 policy of operand loads: 0 normal, 1 evict first,
+  int32_t b_l2;        // 2 evict last
   int32_t* status;     // device status word (FLCE_DEV_* bits)
 };
+
+// Tile t of a launch -> (m block, n block).  The CTAs that run at the same
+// time cover a band of consecutive tiles: the fastest index sweeps its whole
+// operand, which should fit in L2 and stay resident, while the operand of
+// the slow index streams through once.
+__host__ __device__ inline void tile_coords(const GemmGrid& g, int tile, int& m_blk, int& n_blk) {
+  if (g.raster_n) {
+    n_blk = tile % g.num_n_blk;
+    m_blk = tile / g.num_n_blk;
+  } else {
+    m_blk = tile % g.num_m_blk;
+    n_blk = tile / g.num_m_blk;
+  }
+}
 
 // Small device-side scalars of one call.
 struct Scalars {

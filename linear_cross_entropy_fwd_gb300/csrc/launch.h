@@ -31,34 +31,38 @@ struct StoreParams {
   int32_t reduce;
 };
 
-// Set the dynamic shared-memory limit of every GEMM kernel on the current device.
-cudaError_t gemm_prepare_bf16();
-cudaError_t gemm_prepare_fp32();
+// Set the dynamic shared-memory limit of every GEMM kernel on the current
+// device; *max_units = scheduling units (bf16: CTA pairs, fp32: CTAs) that
+// fit on the device at once.  Launchers take the number of units to run
+// (each unit walks tiles unit, unit + units, ...; tile M blocks are
+// GemmShape rows: 256 for bf16 pairs, 128 for fp32).
+cudaError_t gemm_prepare_bf16(int sms, int* max_units);
+cudaError_t gemm_prepare_fp32(int sms, int* max_units);
 
 // Pass 1: A = X (K-major), B = W (K-major), epilogue = per-tile row statistics.
 cudaError_t launch_logits_lse_bf16(const CUtensorMap& A, const CUtensorMap& B, const GemmGrid& g,
-                                   const RowLseParams& p, int grid, cudaStream_t s);
+                                   const RowLseParams& p, int units, cudaStream_t s);
 cudaError_t launch_logits_lse_fp32(const CUtensorMap& A, const CUtensorMap& B, const GemmGrid& g,
-                                   const RowLseParams& p, int grid, cudaStream_t s);
+                                   const RowLseParams& p, int units, cudaStream_t s);
 // Pass 2: A = X (K-major), B = W chunk (K-major), epilogue = G chunk store.
 cudaError_t launch_logits_grad_bf16(const CUtensorMap& A, const CUtensorMap& B,
                                     const CUtensorMap& out, const GemmGrid& g,
-                                    const GradLogitsParams& p, int grid, cudaStream_t s);
+                                    const GradLogitsParams& p, int units, cudaStream_t s);
 cudaError_t launch_logits_grad_fp32(const CUtensorMap& A, const CUtensorMap& B,
                                     const CUtensorMap& out, const GemmGrid& g,
-                                    const GradLogitsParams& p, int grid, cudaStream_t s);
+                                    const GradLogitsParams& p, int units, cudaStream_t s);
 // dW chunk: A = G^T, B = X (bf16: both MN-major views of G and X; fp32:
 // K-major transposed copies G^T [Vc, N] and X^T [H, N]), fp32 store.
 cudaError_t launch_dw_bf16(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& out,
-                           const GemmGrid& g, const StoreParams& p, int grid, cudaStream_t s);
+                           const GemmGrid& g, const StoreParams& p, int units, cudaStream_t s);
 cudaError_t launch_dw_fp32(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& out,
-                           const GemmGrid& g, const StoreParams& p, int grid, cudaStream_t s);
+                           const GemmGrid& g, const StoreParams& p, int units, cudaStream_t s);
 // dX chunk: A = G (K-major), B = W chunk (bf16: MN-major view of W; fp32:
 // K-major transposed copy W_c^T [H, Vc]), fp32 store or add.
 cudaError_t launch_dx_bf16(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& out,
-                           const GemmGrid& g, const StoreParams& p, int grid, cudaStream_t s);
+                           const GemmGrid& g, const StoreParams& p, int units, cudaStream_t s);
 cudaError_t launch_dx_fp32(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& out,
-                           const GemmGrid& g, const StoreParams& p, int grid, cudaStream_t s);
+                           const GemmGrid& g, const StoreParams& p, int units, cudaStream_t s);
 
 // Row combine: partial statistics -> lse2, row losses, mean loss, n_valid, scale.
 struct CombineParams {
