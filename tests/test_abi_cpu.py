@@ -66,8 +66,11 @@ def test_workspace_plans(lib):
     a = flce.flce_workspace_bytes(8192, 4096, 128256, vocab_chunk=1024)
     b = flce.flce_workspace_bytes(8192, 4096, 128256, vocab_chunk=2048)
     assert b - a == 8192 * 1024 * 2
+    # a budget below what a 2048-column chunk needs gets the 2048-column plan
     small = flce.flce_workspace_bytes(8192, 4096, 128256, workspace_budget=150 * 2 ** 20)
-    assert small <= 150 * 2 ** 20 + 8192 * 256 * 2
+    assert small == flce.flce_workspace_bytes(8192, 4096, 128256, vocab_chunk=2048)
+    mid = flce.flce_workspace_bytes(8192, 4096, 128256, workspace_budget=200 * 2 ** 20)
+    assert small < mid <= 200 * 2 ** 20
     # bad sizes plan nothing
     assert flce.flce_workspace_bytes(10, 0, 5) == 0
     assert flce.flce_workspace_bytes(10, 8, 5, vocab_chunk=300) == 0
