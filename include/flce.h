@@ -189,6 +189,41 @@ FLCE_API int flce_version(void);
  * mirror of the struct). */
 FLCE_API size_t flce_opts_sizeof(void);
 
+/*
+ * Loss-only pass (the work of flce_fwd) that allocates no device memory.
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that cannot call cudaMalloc at the point where the loss is needed: a host
+ * application that plans all device memory up front in its own arena, a
+ * plugin whose execute step may not allocate, or a latency-bound loop where
+ * an allocation could synchronise the device or fail under fragmentation.
+ *
+ * Its scratch space is a static device array inside libflce of
+ * 32 MiB (33554432 bytes); every device the library runs on holds it until
+ * the process exits.  A problem whose loss-only plan needs more (about
+ * 4 * N * ceil(V / 256) + 8 * N bytes plus a few KB; flce_workspace_bytes()
+ * with with_grads = 0 gives the exact figure) is rejected with
+ * FLCE_ERR_WORKSPACE before anything is launched.
+ *
+ *   X [N, H], W [V, H] of element type `dtype` (FLCE_BF16 or FLCE_FP32),
+ *   target [N] int64: device inputs, read only.
+ *   loss_dev (required), lse_out [N], n_valid_dev, status_dev: device outputs
+ *   as in flce_opts (NULL skips the optional ones); status_dev receives the
+ *   kernels' flce_status (bad targets, expired waits).
+ *   stream: cudaStream_t to launch on (NULL = legacy default stream).
+ * The call is asynchronous: results are valid once `stream` reaches them.
+ *
+ * The first call on a device looks up the device address of the static
+ * array with cudaGetSymbolAddress (once per device, with that device
+ * current); make that first call before any stream capture.  All calls share
+ * the one array and each leaves its contents behind: calls that may overlap
+ * on the GPU (different streams or host threads without ordering between
+ * them) race on it and must be serialised by the caller.
+ */
+FLCE_API int flce_fwd_noalloc(const void* X, const void* W, const int64_t* target, int64_t N,
+                              int64_t H, int64_t V, int64_t ignore_index, int32_t dtype,
+                              float* loss_dev, float* lse_out, int64_t* n_valid_dev,
+                              int32_t* status_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

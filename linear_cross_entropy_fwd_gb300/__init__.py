@@ -32,7 +32,7 @@ TRACE_KINDS = {1: "logits_lse", 2: "combine", 3: "logits_grad", 4: "dw", 5: "dx"
 
 EXPORTED = ["flce_opts_init", "flce_fwd_bwd", "flce_fwd_bwd_ex", "flce_fwd",
             "flce_fwd_bwd_host", "flce_workspace_bytes", "flce_status_str",
-            "flce_last_error", "flce_version", "flce_opts_sizeof"]
+            "flce_last_error", "flce_version", "flce_opts_sizeof", "flce_fwd_noalloc"]
 
 
 class FlceOpts(ctypes.Structure):
@@ -106,6 +106,8 @@ def load_library(path: str | None = None):
         lib.flce_version.restype = i32
         lib.flce_opts_sizeof.argtypes = []
         lib.flce_opts_sizeof.restype = ctypes.c_size_t
+        lib.flce_fwd_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i32, vp, vp, vp, vp, vp]
+        lib.flce_fwd_noalloc.restype = i32
         if lib.flce_opts_sizeof() != ctypes.sizeof(FlceOpts):
             raise RuntimeError("flce_opts layout mismatch between libflce and the binding")
         _lib = lib
@@ -266,6 +268,38 @@ def flce_fwd(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor, ignore_inde
     if info is not None:
         info.update(workspace_bytes=used.value, status=status)
     return loss, nval
+
+
+def flce_fwd_noalloc(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor,
+                     ignore_index: int = -100, *, loss: torch.Tensor | None = None,
+                     lse_out: torch.Tensor | None = None, n_valid: torch.Tensor | None = None,
+                     status: torch.Tensor | None = None):
+    """Loss only, through the entry point that allocates no device memory
+    inside the library (its scratch is a fixed 32 MiB static array; larger
+    problems raise FlceError with FLCE_ERR_WORKSPACE).  For callers that plan
+    device memory up front and cannot allocate at this point; pass
+    preallocated ``loss`` (0-d fp32), ``n_valid`` (0-d int64) and ``status``
+    (0-d int32) to keep the call itself allocation-free.  Calls share the
+    library's scratch, so calls that may overlap on the GPU must be
+    serialised.  Returns (loss, n_valid, status) device tensors."""
+    lib = load_library()
+    _check_inputs(X, W, target)
+    N, H = X.shape
+    V = W.shape[0]
+    dev = X.device
+    if loss is None:
+        loss = torch.empty((), dtype=torch.float32, device=dev)
+    if n_valid is None:
+        n_valid = torch.empty((), dtype=torch.int64, device=dev)
+    if status is None:
+        status = torch.empty((), dtype=torch.int32, device=dev)
+    st = lib.flce_fwd_noalloc(X.data_ptr(), W.data_ptr(), target.data_ptr(), N, H, V,
+                              int(ignore_index), _dtype_code(X), loss.data_ptr(),
+                              None if lse_out is None else lse_out.data_ptr(),
+                              n_valid.data_ptr(), status.data_ptr(),
+                              torch.cuda.current_stream(dev).cuda_stream)
+    _check(st)
+    return loss, n_valid, status
 
 
 def flce_fwd_bwd_host(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor,

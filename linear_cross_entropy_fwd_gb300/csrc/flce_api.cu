@@ -540,6 +540,44 @@ int entry(const void* X, const void* W, const int64_t* target, int64_t N, int64_
 }  // namespace
 }  // namespace flce
 
+// ------------------------------------------------ allocation-free loss entry
+// Scratch of flce_fwd_noalloc(): a fixed device array owned by this library.
+// Every device on which the library runs a kernel holds it until the process
+// exits.  Host code must not pass `g_noalloc_scratch` itself to a kernel (on
+// the host that name is only a stand-in for the device symbol); its device
+// address comes from cudaGetSymbolAddress() below.
+constexpr size_t kNoAllocScratchBytes = size_t{32} << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace flce {
+namespace {
+
+void* g_noalloc_addr[kMaxDevices] = {};
+std::mutex g_noalloc_mutex;
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the lookup may load the library's kernels onto the device).
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  FLCE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_error("device ordinal %d out of range", dev);
+    return FLCE_ERR_ARG;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return FLCE_OK;
+}
+
+}  // namespace
+}  // namespace flce
+
 using namespace flce;
 
 extern "C" {
@@ -650,5 +688,45 @@ const char* flce_last_error(void) { return g_last_error; }
 int flce_version(void) { return FLCE_VERSION; }
 
 size_t flce_opts_sizeof(void) { return sizeof(flce_opts); }
+
+int flce_fwd_noalloc(const void* X, const void* W, const int64_t* target, int64_t N, int64_t H,
+                     int64_t V, int64_t ignore_index, int32_t dtype, float* loss_dev,
+                     float* lse_out, int64_t* n_valid_dev, int32_t* status_dev, void* stream) {
+  g_last_error[0] = 0;
+  flce_opts o;
+  flce_opts_init(&o);
+  o.dtype = dtype;
+  o.sync = 0;
+  o.stream = stream;
+  o.loss_dev = loss_dev;
+  o.lse_out = lse_out;
+  o.n_valid_dev = n_valid_dev;
+  o.status_dev = status_dev;
+  if (!loss_dev) {
+    set_error("loss_dev is null");
+    return FLCE_ERR_ARG;
+  }
+  int rc = check_args(X, W, target, N, H, V, o);
+  if (rc) return rc;
+  DeviceInfo D;
+  if ((rc = device_info(o.dtype, &D))) return rc;
+  Plan P;
+  if ((rc = make_plan(&P, N, H, V, false, o, 0))) return rc;
+  if (P.total > kNoAllocScratchBytes) {
+    set_error("flce_fwd_noalloc: this problem needs %zu bytes of scratch, more than the %zu "
+              "bytes of the library's static scratch array",
+              P.total, kNoAllocScratchBytes);
+    return FLCE_ERR_WORKSPACE;
+  }
+  void* ws = nullptr;
+  if ((rc = noalloc_scratch(&ws))) return rc;
+  o.workspace = ws;
+  o.workspace_bytes = kNoAllocScratchBytes;
+  // run_path clears the words that must start at zero (status, the combine's
+  // ticket) on the stream before its first kernel; every other scratch byte
+  // is written before it is read.
+  return run_path(P, D, X, W, target, ignore_index, nullptr, nullptr,
+                  static_cast<uint8_t*>(ws), o, static_cast<cudaStream_t>(stream));
+}
 
 }  // extern "C"
