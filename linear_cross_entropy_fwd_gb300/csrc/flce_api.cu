@@ -178,6 +178,41 @@ size_t fixed_bytes(Plan& p) {
 }
 
 constexpr int64_t kMinChunk = 2048;
+// Scheduling units the planner assumes (GB300: 152 SMs = 76 CTA pairs), so
+// that a plan, and flce_workspace_bytes(), do not depend on which device
+// (if any) is current when it is made.
+constexpr int64_t kPlanUnitsPair = 76, kPlanUnitsSingle = 152;
+// Per-launch cost the planner charges (ramp-up, last epilogue, launch gap),
+// in 128-byte K blocks of one tile (one K block of a pair tile is ~0.27 us):
+// about 7 us, as measured between chunk widths 4864 and 6656.
+constexpr int64_t kPlanLaunchCost = 26;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Estimated time of the chunk loop for chunk width Vc, in K blocks of one
+// unit: each GEMM launch costs (waves of tiles) x (K blocks per tile) plus a
+// fixed launch cost.  Captures wave quantisation: a chunk whose dW tiles fill
+// 5.5 waves costs as much as 6.
+int64_t chunk_loop_cost(int64_t N, int64_t H, int64_t V, int64_t Vc, int elt, bool pair) {
+  const int64_t U = pair ? kPlanUnitsPair : kPlanUnitsSingle;
+  const int64_t mb = pair ? 2 * BM : BM, ke = 128 / elt;
+  const int64_t mp = ceil_div(N, mb), nh = ceil_div(H, BN);
+  const int64_t kH = ceil_div(H, ke), kN = ceil_div(N, ke);
+  int64_t cost = 0;
+  for (int64_t c0 = 0; c0 < V; c0 += Vc) {
+    const int64_t vc = (V - c0) < Vc ? (V - c0) : Vc;
+    const int64_t nb = ceil_div(vc, BN);
+    cost += ceil_div(mp * nb, U) * kH;                    // pass 2 (G chunk)
+    cost += ceil_div(ceil_div(vc, mb) * nh, U) * kN;      // dW chunk
+    cost += ceil_div(mp * nh, U) * ceil_div(vc, ke);      // dX chunk
+    cost += 3 * kPlanLaunchCost;
+    // chunks after the first add into the fp32 dX accumulator: 8 bytes of
+    // traffic per element, partly hidden under the MMAs (about 70 K blocks
+    // at N x H = 8192 x 4096, in proportion elsewhere)
+    if (c0 > 0) cost += 70 * N * H / (int64_t{8192} * 4096);
+  }
+  return cost;
+}
 
 // budget: bytes the plan may use (0 = N*V*4/16).  Returns FLCE_OK or an error.
 int make_plan(Plan* out, int64_t N, int64_t H, int64_t V, bool grads, const flce_opts& o,
@@ -208,11 +243,24 @@ int make_plan(Plan* out, int64_t N, int64_t H, int64_t V, bool grads, const flce
       if (p.dtype == FLCE_FP32)                            // + G^T and W^T columns
         per_col += static_cast<size_t>(p.Np) * 4 + static_cast<size_t>(H) * 4;
       const size_t avail = budget > fixed ? budget - fixed : 0;
-      Vc = static_cast<int64_t>(avail / per_col) / BN * BN;
+      int64_t vmax = static_cast<int64_t>(avail / per_col) / BN * BN;
       // Narrower chunks cost more than they save: below kMinChunk columns the
       // dW GEMM has too few tiles to fill the GPU, so the budget is exceeded
       // rather than going below it.
-      if (Vc < kMinChunk) Vc = kMinChunk;
+      if (vmax < kMinChunk) vmax = kMinChunk;
+      if (vmax > vpad) vmax = vpad;
+      // Among the widths the budget allows, the one with the least estimated
+      // time (ties: the widest, i.e. the fewest launches).
+      const bool pair = (p.dtype == FLCE_BF16);
+      Vc = vmax;
+      int64_t best = chunk_loop_cost(N, H, V, vmax, p.elt, pair);
+      for (int64_t w = vmax - BN; w >= kMinChunk; w -= BN) {
+        const int64_t cst = chunk_loop_cost(N, H, V, w, p.elt, pair);
+        if (cst < best) {
+          best = cst;
+          Vc = w;
+        }
+      }
     }
     if (Vc > vpad) Vc = vpad;
     p.Vc = Vc;

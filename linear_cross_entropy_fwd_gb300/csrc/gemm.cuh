@@ -132,6 +132,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (PAIR) cluster_sync();  // the peer's barriers exist before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_base_slot;
+  // Everything above touched only this CTA's shared memory and TMEM, so with
+  // programmatic dependent launch it overlaps the previous kernel's tail.
+  // Every global access comes after this wait.  The grid is persistent (never
+  // more units than fit at once), so the next launch may be released at once:
+  // its CTAs take SMs only as this launch's CTAs exit.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

@@ -41,7 +41,7 @@ struct Kernels {
       return cudaSuccess;
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     fill_config(&cfg, attr, sms, nullptr);
     int clusters = 0;
     if ((e = cudaOccupancyMaxActiveClusters(&clusters, lse, &cfg)) != cudaSuccess) return e;
@@ -59,8 +59,13 @@ struct Kernels {
     attr[0].val.clusterDim.x = kPair ? 2 : 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic dependent launch: the kernel's prologue overlaps the tail
+    // of the previous kernel in the stream (the kernel waits on its
+    // predecessor with griddepcontrol.wait before touching global memory)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg->attrs = attr;
-    cfg->numAttrs = 1;
+    cfg->numAttrs = 2;
   }
 
   template <class KernelT, class P>
@@ -68,7 +73,7 @@ struct Kernels {
                             const CUtensorMap& out, const GemmGrid& g, const P& p, int units,
                             cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     fill_config(&cfg, attr, units, s);
     return cudaLaunchKernelEx(&cfg, k, A, B, out, g, p);
   }
