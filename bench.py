@@ -199,6 +199,66 @@ def run_reference(args, workload):
     return 0
 
 
+def run_ce_logits(args, w):
+    """Cross-entropy on materialised bf16 logits [N, V] (loss + gradient into
+    a separate buffer).  HBM-bound: the roofline is bytes moved per launch of
+    the row kernel (one read and one write of the logits) over its time."""
+    import torch
+
+    import linear_cross_entropy_fwd_gb300 as flce
+    from flce_synth import make_inputs
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    flce.load_library()
+    peaks, peak_src = load_peaks()
+    X, W, t = make_inputs(w)
+    S = (X.to(dev) @ W.to(dev).t()).contiguous()  # input staging (cuBLAS), not timed
+    td = t.to(dev)
+    dS = torch.empty_like(S)
+    del X, W
+    for _ in range(max(args.warmup, 1)):
+        flce.flce_ce_fwd_bwd(S, td, w.ignore_index, dlogits=dS)
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(None)
+    sampler.start()
+    time.sleep(0.3)
+    e0.record(stream)
+    for _ in range(args.steps):
+        flce.flce_ce_fwd_bwd(S, td, w.ignore_index, dlogits=dS)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    traces = [flce.Trace(capacity=8) for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for k in range(args.steps):
+        flce.flce_ce_fwd_bwd(S, td, w.ignore_index, dlogits=dS, trace=traces[k])
+    torch.cuda.synchronize(dev)
+    rows_ms = [t_ms for tr in traces for kind, t_ms in tr.launches() if kind == "ce_rows"]
+    rows_avg = sum(rows_ms) / len(rows_ms)
+    elt = S.element_size()
+    algo_bytes = 2.0 * w.N * w.V * elt + w.N * (8 + 8)  # logits in, gradient out, target, stats
+    achieved = algo_bytes / (rows_avg * 1e-3) / 1e9
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    line = {
+        "metric": "tokens/s, cross-entropy on materialised logits (loss + gradient), 1 GB300",
+        "value": w.N / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (logits = X W^T of the workload)",
+        "config": workload_config(w, 1),
+        "roofline": {"bound": "hbm", "kernel": "ce_rows", "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_kind": f"HBM copy ({peak_src})", "bytes_per_launch": algo_bytes,
+                     "traffic": recorded_traffic("ce_rows", w.name)},
+        "gpu_launches": 4 * args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def workload_config(w, n_gpus):
     return {"workload": w.name, "N": w.N, "H": w.H, "V": w.V, "input_dtype": w.dtype,
             "ignored_rows": w.n_ignored, "targets": w.t_dist,
@@ -212,6 +272,9 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="flce", choices=["flce", "reference"])
+    ap.add_argument("--op", default="flce", choices=["flce", "ce_logits"],
+                    help="flce: the fused path (default); ce_logits: cross-entropy on "
+                         "logits already in HBM (logits = X W^T of the workload, bf16)")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--shape", default=None,
                     help="N,H,V: a synthetic case of that size with the workload's recipe "
@@ -233,6 +296,8 @@ def main():
         workload = replace(workload, name=f"custom_{n_}x{h_}x{v_}", N=n_, H=h_, V=v_)
     if args.impl == "reference":
         return run_reference(args, workload)
+    if args.op == "ce_logits":
+        return run_ce_logits(args, workload)
 
     import torch
     import torch.distributed as dist

@@ -80,7 +80,9 @@ typedef enum flce_trace_kind {
   FLCE_TRACE_LOGITS_GRAD = 3,  /* pass 2: logit tiles -> G chunk */
   FLCE_TRACE_DW = 4,           /* dW[chunk] = G_chunk^T X */
   FLCE_TRACE_DX = 5,           /* dX += G_chunk W[chunk] */
-  FLCE_TRACE_CONVERT = 6       /* fp32 dX accumulator -> bf16 dX */
+  FLCE_TRACE_CONVERT = 6,      /* fp32 dX accumulator -> bf16 dX */
+  FLCE_TRACE_CE_COUNT = 7,     /* cross-entropy on logits: valid-row count */
+  FLCE_TRACE_CE_ROWS = 8       /* cross-entropy on logits: row statistics + gradient */
 } flce_trace_kind;
 
 /*
@@ -157,6 +159,26 @@ FLCE_API int flce_fwd_bwd_ex(const void* X, const void* W, const int64_t* target
  */
 FLCE_API int flce_fwd(const void* X, const void* W, const int64_t* target, int64_t N, int64_t H,
              int64_t V, int64_t ignore_index, float* loss, const flce_opts* opts);
+
+/*
+ * Cross-entropy on logits that are already materialised in device memory
+ * (the overview's LigerCrossEntropyLoss, "Kernels Básicos"; in-place
+ * gradient as in "Operações In-Place"): the same loss and reductions as
+ * above with S given directly.
+ *   logits [N, V] of element type opts->dtype (bf16 or fp32), row-major
+ *   target [N] int64;   loss: host float*, or NULL when opts->sync == 0
+ *   dlogits [N, V], same type: dS = valid (softmax - onehot) * grad_scale / n;
+ *   it may be the logits buffer itself (the gradient overwrites the logits,
+ *   each element after it has been read); NULL computes the loss only.
+ * Optional outputs and error reporting as for flce_fwd_bwd_ex (lse_out,
+ * loss_rows_out, loss_dev, n_valid_dev, status_dev, trace).  The scratch
+ * space is 12 N bytes plus a few KB.  Memory traffic: one read of the logits
+ * from HBM and, with a gradient, one write (the second read of each row
+ * comes from L2).
+ */
+FLCE_API int flce_ce_fwd_bwd(const void* logits, const int64_t* target, int64_t N, int64_t V,
+                             int64_t ignore_index, float* loss, void* dlogits,
+                             const flce_opts* opts);
 
 /*
  * End-to-end variant on HOST buffers: copies X, W and target to the device,

@@ -28,11 +28,12 @@ FLCE_OK, FLCE_ERR_ARG, FLCE_ERR_ALIGN, FLCE_ERR_ARCH, FLCE_ERR_TARGET, \
     FLCE_ERR_WORKSPACE, FLCE_ERR_CUDA, FLCE_ERR_TIMEOUT = range(8)
 FLCE_BF16, FLCE_FP32 = 0, 1
 TRACE_KINDS = {1: "logits_lse", 2: "combine", 3: "logits_grad", 4: "dw", 5: "dx",
-               6: "convert"}
+               6: "convert", 7: "ce_count", 8: "ce_rows"}
 
 EXPORTED = ["flce_opts_init", "flce_fwd_bwd", "flce_fwd_bwd_ex", "flce_fwd",
             "flce_fwd_bwd_host", "flce_workspace_bytes", "flce_status_str",
-            "flce_last_error", "flce_version", "flce_opts_sizeof", "flce_fwd_noalloc"]
+            "flce_last_error", "flce_version", "flce_opts_sizeof", "flce_fwd_noalloc",
+            "flce_ce_fwd_bwd"]
 
 
 class FlceOpts(ctypes.Structure):
@@ -108,6 +109,8 @@ def load_library(path: str | None = None):
         lib.flce_opts_sizeof.restype = ctypes.c_size_t
         lib.flce_fwd_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i32, vp, vp, vp, vp, vp]
         lib.flce_fwd_noalloc.restype = i32
+        lib.flce_ce_fwd_bwd.argtypes = [vp, vp, i64, i64, i64, fp, vp, po]
+        lib.flce_ce_fwd_bwd.restype = i32
         if lib.flce_opts_sizeof() != ctypes.sizeof(FlceOpts):
             raise RuntimeError("flce_opts layout mismatch between libflce and the binding")
         _lib = lib
@@ -302,6 +305,61 @@ def flce_fwd_noalloc(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor,
     return loss, n_valid, status
 
 
+def flce_ce_fwd_bwd(logits: torch.Tensor, target: torch.Tensor, ignore_index: int = -100, *,
+                    grad: bool = True, inplace: bool = False,
+                    dlogits: torch.Tensor | None = None, sync: bool = False,
+                    grad_scale: float = 1.0, norm_count: int = 0,
+                    lse_out: torch.Tensor | None = None,
+                    loss_rows_out: torch.Tensor | None = None, trace=None,
+                    info: dict | None = None):
+    """Cross-entropy on logits already in device memory [N, V] (bf16 or fp32).
+
+    Returns (loss 0-d device tensor, n_valid 0-d int64, dlogits or None).
+    ``inplace=True`` writes the gradient over ``logits``."""
+    lib = load_library()
+    if logits.dim() != 2 or target.dim() != 1 or logits.shape[0] != target.shape[0]:
+        raise ValueError("logits [N, V], target [N]")
+    if not (logits.is_cuda and target.is_cuda and logits.is_contiguous()
+            and target.is_contiguous()):
+        raise ValueError("contiguous CUDA tensors expected")
+    if target.dtype != torch.int64:
+        raise TypeError("target must be int64")
+    N, V = logits.shape
+    dev = logits.device
+    if grad:
+        if inplace:
+            dlogits = logits
+        elif dlogits is None:
+            dlogits = torch.empty_like(logits)
+    else:
+        dlogits = None
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    nval = torch.empty((), dtype=torch.int64, device=dev)
+    status = torch.zeros((), dtype=torch.int32, device=dev)
+    o = make_opts(logits.dtype, torch.cuda.current_stream(dev).cuda_stream,
+                  sync=1 if sync else 0, grad_scale=float(grad_scale),
+                  norm_count=int(norm_count))
+    o.dtype = _dtype_code(logits)
+    o.loss_dev = loss.data_ptr()
+    o.n_valid_dev = nval.data_ptr()
+    o.status_dev = status.data_ptr()
+    if lse_out is not None:
+        o.lse_out = lse_out.data_ptr()
+    if loss_rows_out is not None:
+        o.loss_rows_out = loss_rows_out.data_ptr()
+    used = ctypes.c_size_t(0)
+    o.workspace_used = ctypes.pointer(used)
+    keep = _attach_trace(o, trace)
+    st = lib.flce_ce_fwd_bwd(logits.data_ptr(), target.data_ptr(), N, V, int(ignore_index),
+                             None, None if dlogits is None else dlogits.data_ptr(),
+                             ctypes.byref(o))
+    del keep
+    _check(st)
+    if info is not None:
+        info.update(workspace_bytes=used.value, status=status)
+    return loss, nval, dlogits
+
+
 def flce_fwd_bwd_host(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor,
                       ignore_index: int = -100, *, dX: torch.Tensor | None = None,
                       dW: torch.Tensor | None = None, stream=None):
@@ -377,6 +435,31 @@ class _FLCEFunction(torch.autograd.Function):
         dX, dW = ctx.saved_tensors
         gW = (dW * grad_out).to(dX.dtype) if dX.dtype != torch.float32 else dW * grad_out
         return gW, dX * grad_out.to(dX.dtype), None, None
+
+
+class _CEFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, logits, target, ignore_index):
+        loss, _, dS = flce_ce_fwd_bwd(logits.contiguous(), target.contiguous(), ignore_index)
+        ctx.save_for_backward(dS)
+        return loss
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        (dS,) = ctx.saved_tensors
+        return dS * grad_out.to(dS.dtype), None, None
+
+
+class CrossEntropyLoss(torch.nn.Module):
+    """loss_fn(logits, target) on logits already materialised (mean over
+    non-ignored rows); forward computes the gradient as well."""
+
+    def __init__(self, ignore_index: int = -100):
+        super().__init__()
+        self.ignore_index = ignore_index
+
+    def forward(self, logits, target):
+        return _CEFunction.apply(logits, target, self.ignore_index)
 
 
 class LinearCrossEntropyLoss(torch.nn.Module):

@@ -585,6 +585,136 @@ int entry(const void* X, const void* W, const int64_t* target, int64_t N, int64_
   return FLCE_OK;
 }
 
+// Cross-entropy on materialised logits: count, rows, combine.
+int ce_entry(const void* logits, const int64_t* target, int64_t N, int64_t V,
+             int64_t ignore_index, float* loss_host, void* dlogits, const flce_opts* opts_in) {
+  g_last_error[0] = 0;
+  flce_opts o;
+  flce_opts_init(&o);
+  if (opts_in) o = *opts_in;
+  if (N < 0 || V <= 0 || (N > 0 && (!logits || !target))) {
+    set_error("bad arguments (need N >= 0, V > 0 and non-null logits and target)");
+    return FLCE_ERR_ARG;
+  }
+  if (o.dtype != FLCE_BF16 && o.dtype != FLCE_FP32) {
+    set_error("unknown dtype %d", o.dtype);
+    return FLCE_ERR_ARG;
+  }
+  if (N > (int64_t{1} << 31) || V > (int64_t{1} << 31)) {
+    set_error("size too large (N, V <= 2^31)");
+    return FLCE_ERR_ARG;
+  }
+  const int elt = (o.dtype == FLCE_FP32) ? 4 : 2;
+  DeviceInfo D;
+  int rc = device_info(o.dtype, &D);
+  if (rc) return rc;
+  const bool sync = o.sync != 0 || loss_host != nullptr;
+  const int cgrid = combine_grid(N);
+  size_t off = 0;
+  const size_t off_sc = off;
+  off += align_up(sizeof(Scalars), 256);
+  const size_t off_bl = off;
+  off += align_up(static_cast<size_t>(cgrid) * 8, 256);
+  const size_t off_bc = off;
+  off += align_up(static_cast<size_t>(cgrid) * 8, 256);
+  const size_t off_lse2 = off;
+  off += align_up(static_cast<size_t>(N) * 4, 256);
+  const size_t off_st = off;
+  off += align_up(static_cast<size_t>(N) * 4, 256);
+  const size_t off_part = off;
+  off += align_up(static_cast<size_t>(N) * 4, 256);
+  const size_t total = off;
+  if (o.workspace_used) *o.workspace_used = total;
+  if (o.workspace && o.workspace_bytes < total) {
+    set_error("workspace of %zu bytes is smaller than the %zu bytes this call needs",
+              o.workspace_bytes, total);
+    return FLCE_ERR_WORKSPACE;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(o.stream);
+  uint8_t* ws = static_cast<uint8_t*>(o.workspace);
+  bool owned = false;
+  if (!ws) {
+    void* pws = nullptr;
+    FLCE_CUDA(cudaMallocAsync(&pws, total, s));
+    ws = static_cast<uint8_t*>(pws);
+    owned = true;
+  }
+  Scalars* sc = reinterpret_cast<Scalars*>(ws + off_sc);
+  Tracer tr(o, s);
+  cudaError_t e = cudaMemsetAsync(sc, 0, sizeof(Scalars), s);
+  if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemsetAsync(scalars)");
+  if (rc == FLCE_OK) rc = tr.start();
+  if (rc == FLCE_OK && N > 0) {
+    e = launch_ce_count(target, N, V, ignore_index, sc, D.sms, s);
+    if (e != cudaSuccess) rc = cuda_fail(e, "ce_count");
+    if (rc == FLCE_OK) rc = tr.after(FLCE_TRACE_CE_COUNT);
+  }
+  if (rc == FLCE_OK && N > 0) {
+    CeRowsParams cp{};
+    cp.logits = logits;
+    cp.dlogits = dlogits;
+    cp.target = target;
+    cp.N = N;
+    cp.V = V;
+    cp.ignore_index = ignore_index;
+    cp.sc = sc;
+    cp.grad_scale = o.grad_scale;
+    cp.norm_count = o.norm_count;
+    cp.partial = reinterpret_cast<float*>(ws + off_part);
+    cp.st = reinterpret_cast<float*>(ws + off_st);
+    cp.vectorized = ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(dlogits)) &
+                     15u) == 0 &&
+                    (V * elt) % 16 == 0;
+    e = launch_ce_rows(cp, elt, D.sms, s);
+    if (e != cudaSuccess) rc = cuda_fail(e, "ce_rows");
+    if (rc == FLCE_OK) rc = tr.after(FLCE_TRACE_CE_ROWS);
+  }
+  if (rc == FLCE_OK) {
+    CombineParams cp{};
+    cp.partial = reinterpret_cast<float*>(ws + off_part);
+    cp.num_vblk = 1;
+    cp.st = reinterpret_cast<float*>(ws + off_st);
+    cp.target = target;
+    cp.N = N;
+    cp.V = V;
+    cp.ignore_index = ignore_index;
+    cp.lse2 = reinterpret_cast<float*>(ws + off_lse2);
+    cp.lse_out = o.lse_out;
+    cp.loss_rows_out = o.loss_rows_out;
+    cp.blk_loss = reinterpret_cast<double*>(ws + off_bl);
+    cp.blk_cnt = reinterpret_cast<int64_t*>(ws + off_bc);
+    cp.sc = sc;
+    cp.grad_scale = o.grad_scale;
+    cp.norm_count = o.norm_count;
+    cp.loss_out = o.loss_dev;
+    cp.nvalid_out = o.n_valid_dev;
+    e = launch_combine(cp, s);
+    if (e != cudaSuccess) rc = cuda_fail(e, "combine");
+    if (rc == FLCE_OK) rc = tr.after(FLCE_TRACE_COMBINE);
+  }
+  if (rc == FLCE_OK && o.status_dev) {
+    e = launch_status_code(sc, o.status_dev, s);
+    if (e != cudaSuccess) rc = cuda_fail(e, "status");
+  }
+  tr.finish();
+  Scalars host_sc{};
+  if (rc == FLCE_OK && sync) {
+    e = cudaMemcpyAsync(&host_sc, sc, sizeof(Scalars), cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemcpyAsync(scalars)");
+  }
+  if (owned) {
+    e = cudaFreeAsync(ws, s);
+    if (e != cudaSuccess && rc == FLCE_OK) rc = cuda_fail(e, "cudaFreeAsync(workspace)");
+  }
+  if (rc != FLCE_OK) return rc;
+  if (sync) {
+    FLCE_CUDA(cudaStreamSynchronize(s));
+    if ((rc = status_from_bits(host_sc.status))) return rc;
+    if (loss_host) *loss_host = host_sc.loss;
+  }
+  return FLCE_OK;
+}
+
 }  // namespace
 }  // namespace flce
 
@@ -736,6 +866,11 @@ const char* flce_last_error(void) { return g_last_error; }
 int flce_version(void) { return FLCE_VERSION; }
 
 size_t flce_opts_sizeof(void) { return sizeof(flce_opts); }
+
+int flce_ce_fwd_bwd(const void* logits, const int64_t* target, int64_t N, int64_t V,
+                    int64_t ignore_index, float* loss, void* dlogits, const flce_opts* opts) {
+  return ce_entry(logits, target, N, V, ignore_index, loss, dlogits, opts);
+}
 
 int flce_fwd_noalloc(const void* X, const void* W, const int64_t* target, int64_t N, int64_t H,
                      int64_t V, int64_t ignore_index, int32_t dtype, float* loss_dev,

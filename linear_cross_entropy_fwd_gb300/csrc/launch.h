@@ -97,6 +97,26 @@ cudaError_t launch_transpose_f32(const float* in, int64_t R, int64_t C, int64_t 
                                  float* out, int64_t out_pitch, int64_t R_pad, int sms,
                                  cudaStream_t s);
 
+// Cross-entropy on materialised logits.
+constexpr int CE_THREADS = 512;
+struct CeRowsParams {
+  const void* logits;     // [N, V] bf16 or fp32
+  void* dlogits;          // [N, V] same type, may equal logits; NULL = loss only
+  const int64_t* target;  // [N]
+  int64_t N;
+  int64_t V;
+  int64_t ignore_index;
+  const Scalars* sc;      // n_valid counted by launch_ce_count
+  float grad_scale;
+  int64_t norm_count;
+  float* partial;         // [N] lse2 per row (the combine's single statistic)
+  float* st;              // [N] target logit
+  int32_t vectorized;     // rows start 16-byte aligned and V * elt % 16 == 0
+};
+cudaError_t launch_ce_count(const int64_t* target, int64_t N, int64_t V, int64_t ignore_index,
+                            Scalars* sc, int sms, cudaStream_t s);
+cudaError_t launch_ce_rows(const CeRowsParams& p, int elt, int sms, cudaStream_t s);
+
 // fp32 [n] -> bf16 [n] (round to nearest even).
 cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t n, int sms, cudaStream_t s);
 

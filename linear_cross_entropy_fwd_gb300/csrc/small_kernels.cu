@@ -2,7 +2,11 @@
 //   * row combine: per-tile row statistics -> lse, row loss, deterministic
 //     mean loss, exact count of valid rows, gradient scale;
 //   * fp32 -> bf16 conversion of the dX accumulator;
-//   * fp32 transposes feeding the tf32 gradient GEMMs K-major operands.
+//   * fp32 transposes feeding the tf32 gradient GEMMs K-major operands;
+//   * cross-entropy on logits already materialised in memory: a count of
+//     the valid rows, then one CTA per row computing the row statistics and
+//     writing the gradient from a second read of the row (normally an L2
+//     hit: the CTAs in flight hold a few tens of MB of rows).
 #include <cuda_runtime.h>
 
 #include "launch.h"
@@ -208,6 +212,236 @@ cudaError_t launch_transpose_f32(const float* in, int64_t R, int64_t C, int64_t 
   if (blocks < 1) blocks = 1;
   transpose_f32_kernel<<<static_cast<unsigned>(blocks), dim3(32, 8), 0, s>>>(
       in, R, C, in_pitch, out, out_pitch, R_pad);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Cross-entropy on materialised logits S [N, V] (bf16 or fp32).
+
+// n_valid (atomic integer adds: exact) and the bad-target flag.
+__global__ void ce_count_kernel(const int64_t* __restrict__ target, int64_t N, int64_t V,
+                                int64_t ignore_index, Scalars* sc) {
+  int cnt = 0;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < N;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = target[i];
+    if (t == ignore_index) continue;
+    if (t < 0 || t >= V)
+      atomicOr(&sc->status, FLCE_DEV_TARGET);
+    else
+      ++cnt;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+  if ((threadIdx.x & 31) == 0 && cnt)
+    atomicAdd(reinterpret_cast<unsigned long long*>(&sc->n_valid),
+              static_cast<unsigned long long>(cnt));
+}
+
+cudaError_t launch_ce_count(const int64_t* target, int64_t N, int64_t V, int64_t ignore_index,
+                            Scalars* sc, int sms, cudaStream_t s) {
+  int64_t blocks = (N + 255) / 256;
+  if (blocks > static_cast<int64_t>(sms) * 4) blocks = static_cast<int64_t>(sms) * 4;
+  if (blocks < 1) blocks = 1;
+  ce_count_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(target, N, V, ignore_index, sc);
+  return cudaGetLastError();
+}
+
+template <int ELT>
+struct CeVec;
+template <>
+struct CeVec<2> {  // 8 bf16 per 16-byte access
+  static constexpr int kPer = 8;
+  __device__ static void unpack(const uint4& u, float* f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      f[2 * k] = __uint_as_float(w[k] << 16);
+      f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  }
+  __device__ static uint4 pack(const float* f) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+  }
+  __device__ static float load1(const void* p, int64_t i) {
+    return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(p)[i]) << 16);
+  }
+  __device__ static void store1(void* p, int64_t i, float v) {
+    static_cast<uint16_t*>(p)[i] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
+  }
+};
+template <>
+struct CeVec<4> {  // 4 fp32 per 16-byte access
+  static constexpr int kPer = 4;
+  __device__ static void unpack(const uint4& u, float* f) {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+  }
+  __device__ static uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+  __device__ static float load1(const void* p, int64_t i) {
+    return static_cast<const float*>(p)[i];
+  }
+  __device__ static void store1(void* p, int64_t i, float v) { static_cast<float*>(p)[i] = v; }
+};
+
+__device__ __forceinline__ void online_add(float& m, float& l, float u) {
+  // u in the log2 domain (logit * log2 e)
+  if (u > m) {
+    l = l * fast_exp2(m - u) + 1.f;
+    m = u;
+  } else {
+    l += fast_exp2(u - m);
+  }
+}
+
+__device__ __forceinline__ void online_merge(float& m, float& l, float m2, float l2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) return;
+  l = (m == -INFINITY ? 0.f : l * fast_exp2(m - M)) + (m2 == -INFINITY ? 0.f : l2 * fast_exp2(m2 - M));
+  m = M;
+}
+
+// CTAs per SM of the row kernel (one row in flight each).  Measured on the
+// 8192 x 128256 case: 1 -> 3.1, 2 -> 3.9, 3 -> 4.3 TB/s (bf16, algorithmic
+// bytes).  With this many rows in flight the second read of a row mostly
+// misses L2 (6.9% hit rate in the profile), so the kernel moves about 1.5x
+// the algorithmic bytes and runs near the HBM copy rate.
+constexpr int kCeCtasPerSm = 3;
+
+// One CTA per row (grid-stride).  Pass A: max and sum of 2^(S log2 e) by an
+// online update per thread, merged across the CTA; lse2 and the target logit
+// go to the row-statistics buffers the combine kernel reads.  Pass B (when
+// dS is wanted): the row again (from L2: it was just read), and
+// dS = valid (2^(S log2 e - lse2) - [j = t]) * grad_scale / n.
+template <int ELT>
+__global__ void __launch_bounds__(CE_THREADS) ce_rows_kernel(const CeRowsParams p) {
+  using Vec = CeVec<ELT>;
+  constexpr float kLog2e = 1.4426950408889634f;
+  __shared__ float s_m[CE_THREADS / 32], s_l[CE_THREADS / 32];
+  __shared__ float s_lse2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool vec = p.vectorized;
+  const int64_t nvec = vec ? p.V / Vec::kPer : 0;
+  const int64_t n = p.norm_count > 0 ? p.norm_count : p.sc->n_valid;
+  const float scale = n > 0 ? static_cast<float>(static_cast<double>(p.grad_scale) /
+                                                 static_cast<double>(n))
+                            : 0.f;
+  for (int64_t r = blockIdx.x; r < p.N; r += gridDim.x) {
+    const uint8_t* row = static_cast<const uint8_t*>(p.logits) + r * p.V * ELT;
+    float m = -INFINITY, l = 0.f;
+    if (vec) {
+      // four independent 16-byte loads in flight per thread
+      const uint4* rv = reinterpret_cast<const uint4*>(row);
+      int64_t k = threadIdx.x;
+      for (; k + 3 * CE_THREADS < nvec; k += 4 * CE_THREADS) {
+        uint4 u[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) u[q] = __ldg(rv + k + q * CE_THREADS);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float f[Vec::kPer];
+          Vec::unpack(u[q], f);
+#pragma unroll
+          for (int e = 0; e < Vec::kPer; ++e) online_add(m, l, f[e] * kLog2e);
+        }
+      }
+      for (; k < nvec; k += CE_THREADS) {
+        float f[Vec::kPer];
+        Vec::unpack(__ldg(rv + k), f);
+#pragma unroll
+        for (int e = 0; e < Vec::kPer; ++e) online_add(m, l, f[e] * kLog2e);
+      }
+    } else {
+      for (int64_t j = threadIdx.x; j < p.V; j += CE_THREADS)
+        online_add(m, l, Vec::load1(row, j) * kLog2e);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+      online_merge(m, l, m2, l2);
+    }
+    if (lane == 0) {
+      s_m[warp] = m;
+      s_l[warp] = l;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float M = s_m[0], L = s_l[0];
+      for (int w = 1; w < CE_THREADS / 32; ++w) online_merge(M, L, s_m[w], s_l[w]);
+      const float lse2 = M + fast_log2(L);
+      s_lse2 = lse2;
+      p.partial[r] = lse2;
+      const int64_t t = p.target[r];
+      p.st[r] = (t >= 0 && t < p.V) ? Vec::load1(row, t) : 0.f;
+    }
+    __syncthreads();
+    if (p.dlogits) {
+      const float lse2 = s_lse2;
+      const int64_t t = p.target[r];
+      const bool valid = (t != p.ignore_index) && t >= 0 && t < p.V;
+      const float sc = valid ? scale : 0.f;
+      uint8_t* out = static_cast<uint8_t*>(p.dlogits) + r * p.V * ELT;
+      if (vec) {
+        const uint4* rv = reinterpret_cast<const uint4*>(row);
+        uint4* ov = reinterpret_cast<uint4*>(out);
+        int64_t k = threadIdx.x;
+        for (; k + 3 * CE_THREADS < nvec; k += 4 * CE_THREADS) {
+          uint4 u[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) u[q] = rv[k + q * CE_THREADS];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float f[Vec::kPer];
+            Vec::unpack(u[q], f);
+            const int64_t kk = k + q * CE_THREADS;
+#pragma unroll
+            for (int e = 0; e < Vec::kPer; ++e) {
+              const int64_t j = kk * Vec::kPer + e;
+              f[e] = valid ? (fast_exp2(fmaf(f[e], kLog2e, -lse2)) - (j == t ? 1.f : 0.f)) * sc
+                           : 0.f;
+            }
+            __stcs(ov + kk, Vec::pack(f));
+          }
+        }
+        for (; k < nvec; k += CE_THREADS) {
+          float f[Vec::kPer];
+          Vec::unpack(rv[k], f);
+#pragma unroll
+          for (int e = 0; e < Vec::kPer; ++e) {
+            const int64_t j = k * Vec::kPer + e;
+            f[e] = valid ? (fast_exp2(fmaf(f[e], kLog2e, -lse2)) - (j == t ? 1.f : 0.f)) * sc
+                         : 0.f;
+          }
+          __stcs(ov + k, Vec::pack(f));
+        }
+      } else {
+        for (int64_t j = threadIdx.x; j < p.V; j += CE_THREADS) {
+          const float x = Vec::load1(row, j);
+          const float g =
+              valid ? (fast_exp2(fmaf(x, kLog2e, -lse2)) - (j == t ? 1.f : 0.f)) * sc : 0.f;
+          Vec::store1(out, j, g);
+        }
+      }
+    }
+    __syncthreads();  // s_m / s_l / s_lse2 are reused by the next row
+  }
+}
+
+cudaError_t launch_ce_rows(const CeRowsParams& p, int elt, int sms, cudaStream_t s) {
+  const int64_t cap = static_cast<int64_t>(sms) * kCeCtasPerSm;
+  int64_t blocks = p.N < cap ? p.N : cap;
+  if (blocks < 1) return cudaSuccess;
+  if (elt == 2)
+    ce_rows_kernel<2><<<static_cast<unsigned>(blocks), CE_THREADS, 0, s>>>(p);
+  else
+    ce_rows_kernel<4><<<static_cast<unsigned>(blocks), CE_THREADS, 0, s>>>(p);
   return cudaGetLastError();
 }
 

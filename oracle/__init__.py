@@ -63,6 +63,8 @@ def _load():
             lib.oracle_flce_dw_rows.argtypes = [p, p, i32, p, i64, i64, i64, i64,
                                                 p, i64, p]
             lib.oracle_flce_dw_rows.restype = i32
+            lib.oracle_ce.argtypes = [p, i32, p, i64, i64, i64, p, p, p, p, p]
+            lib.oracle_ce.restype = i32
             lib.oracle_count_valid.argtypes = [p, i64, i64]
             lib.oracle_count_valid.restype = i64
             lib.oracle_num_threads.argtypes = []
@@ -185,6 +187,25 @@ def flce_dw_rows(X, W, t, vocab_rows, ignore_index: int = -100) -> np.ndarray:
                                      int(ignore_index), _ptr(r), len(r), _ptr(out))
     _check(rc)
     return out
+
+
+def ce(S, t, ignore_index: int = -100, grads: bool = True) -> dict:
+    """Cross-entropy on materialised logits S [N, V]: loss, n_valid, lse,
+    loss_rows, dS [N, V] (the gradient of the mean loss)."""
+    s, ts = _as_matrix(S)
+    tt = _as_targets(t)
+    N, V = s.shape
+    assert tt.shape == (N,)
+    loss = np.zeros(1)
+    nv = np.zeros(1, dtype=np.int64)
+    lse = np.zeros(N)
+    lrows = np.zeros(N)
+    dS = np.zeros((N, V)) if grads else None
+    rc = _load().oracle_ce(_ptr(s), ts, _ptr(tt), N, V, int(ignore_index), _ptr(loss),
+                           _ptr(nv), _ptr(lse), _ptr(lrows), _ptr(dS))
+    _check(rc)
+    return {"loss": float(loss[0]), "n_valid": int(nv[0]), "lse": lse, "loss_rows": lrows,
+            "dS": dS}
 
 
 def count_valid(t, ignore_index: int = -100) -> int:

@@ -279,3 +279,52 @@ int oracle_flce_dw_rows(const void *X, const void *W, int type, const int64_t *t
   free(lse_all);
   return 0;
 }
+
+/*
+ * Cross-entropy on logits that are already materialised (the operator the
+ * overview lists as LigerCrossEntropyLoss, "Kernels Básicos"): the same
+ * definition as above with S given directly as an [N, V] matrix.
+ *   loss = (1/n) sum_{valid i} (lse_i - S_{i,t_i}),
+ *   dS_ij = valid_i (exp(S_ij - lse_i) - [j == t_i]) / n
+ * Outputs: *loss, *n_valid, lse[N], loss_rows[N] (may be NULL), dS[N*V]
+ * (may be NULL).  Element types as for oracle_flce.
+ */
+int oracle_ce(const void *S, int type, const int64_t *t, int64_t N, int64_t V,
+              int64_t ignore_index, double *loss, int64_t *n_valid, double *lse,
+              double *loss_rows, double *dS) {
+  if (N < 0 || V <= 0 || !loss || !n_valid) return 1;
+  if (N > 0 && (!S || !t)) return 1;
+  int rc = check_targets(t, N, V, ignore_index);
+  if (rc) return rc;
+  const int64_t nv = oracle_count_valid(t, N, ignore_index);
+  *n_valid = nv;
+  double *lrow = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+  if (!lrow) return 1;
+#pragma omp parallel
+  {
+    double *srow = (double *)malloc((size_t)V * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t i = 0; i < N; ++i) {
+      for (int64_t j = 0; j < V; ++j) srow[j] = elem(S, type, i * V + j);
+      const double l = logsumexp(srow, V);
+      const int valid = t[i] != ignore_index;
+      if (lse) lse[i] = l;
+      lrow[i] = valid ? l - srow[t[i]] : 0.0;
+      if (dS) {
+        for (int64_t j = 0; j < V; ++j) {
+          double g = 0.0;
+          if (valid && nv > 0)
+            g = (exp(srow[j] - l) - (t[i] == j ? 1.0 : 0.0)) / (double)nv;
+          dS[i * V + j] = g;
+        }
+      }
+    }
+    free(srow);
+  }
+  double acc = 0.0;
+  for (int64_t i = 0; i < N; ++i) acc += lrow[i];
+  *loss = nv > 0 ? acc / (double)nv : 0.0;
+  if (loss_rows) memcpy(loss_rows, lrow, (size_t)N * sizeof(double));
+  free(lrow);
+  return 0;
+}

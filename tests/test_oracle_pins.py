@@ -299,3 +299,45 @@ def test_workload_valid_counts(name):
     assert oracle.count_valid(t, IGN) == GOLDEN["ignored_counts"][name]
     valid = t[t != IGN]
     assert valid.min() >= 0 and valid.max() < w.V
+
+
+# ------------------------------------------------- CE on materialised logits
+def test_ce_zero_logits_is_log_V():
+    """All-zero logits: every valid row's loss is log V, dS = (1/V - onehot)/n."""
+    V = 256
+    S = np.zeros((5, V))
+    t = np.array([0, 255, IGN, 7, 7], dtype=np.int64)
+    r = oracle.ce(S, t, IGN)
+    assert abs(r["loss"] - GOLDEN["log_V"]["256"]) <= 1e-15 * 6
+    expect = np.where((t != IGN)[:, None], np.full((5, V), 1.0 / V), 0.0)
+    for i in range(5):
+        if t[i] != IGN:
+            expect[i, t[i]] -= 1.0
+    np.testing.assert_allclose(r["dS"], expect / 4, rtol=1e-14, atol=1e-18)
+
+
+def test_ce_agrees_with_fused_oracle_through_the_chain_rule():
+    """CE on S = X W^T (formed in float64) equals the fused oracle's loss, and
+    its dS maps to the fused gradients: dX = dS W, dW = dS^T X."""
+    X, W, t = make_case(23, 16, 50, "fp32", seed=51, ignore_num=15, w_std=0.5)
+    Xd, Wd = X.double().numpy(), W.double().numpy()
+    f = oracle.flce(X, W, t, IGN)
+    c = oracle.ce(Xd @ Wd.T, t, IGN)
+    assert abs(c["loss"] - f["loss"]) <= 1e-13
+    assert c["n_valid"] == f["n_valid"]
+    np.testing.assert_allclose(c["lse"], f["lse"], rtol=1e-14)
+    np.testing.assert_allclose(c["dS"] @ Wd, f["dX"], rtol=1e-11, atol=1e-16)
+    np.testing.assert_allclose(c["dS"].T @ Xd, f["dW"], rtol=1e-11, atol=1e-16)
+
+
+def test_ce_against_torch_cross_entropy():
+    S = torch.randn(40, 300, dtype=torch.float64, generator=torch.Generator().manual_seed(5)) * 3
+    t = torch.randint(0, 300, (40,), generator=torch.Generator().manual_seed(6))
+    t[::7] = IGN
+    r = oracle.ce(S, t, IGN)
+    Sg = S.clone().requires_grad_(True)
+    loss = torch.nn.functional.cross_entropy(Sg, t, ignore_index=IGN)
+    loss.backward()
+    assert abs(r["loss"] - loss.item()) <= 1e-12 * loss.item()
+    np.testing.assert_allclose(r["dS"], Sg.grad.numpy(), rtol=1e-10, atol=1e-16)
+    np.testing.assert_allclose(r["dS"].sum(axis=1), 0.0, atol=1e-15)
