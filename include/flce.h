@@ -212,6 +212,17 @@ FLCE_API int flce_version(void);
 FLCE_API size_t flce_opts_sizeof(void);
 
 /*
+ * Self-test of the kernels' bounded waits (the failure-detection path of
+ * every kernel in this library): one block waits on an mbarrier that nothing
+ * will arrive on.  The wait must give up after limit_ns nanoseconds (at most
+ * 2e9), record the expiry in the status word and let the kernel end
+ * normally; the call then returns FLCE_ERR_TIMEOUT, the context stays
+ * usable, and later calls work.  Returns FLCE_OK only if the wait did not
+ * expire (a fault in the mechanism).  Synchronous; allocates a few bytes.
+ */
+FLCE_API int flce_selftest_wait_expiry(int64_t limit_ns);
+
+/*
  * Loss-only pass (the work of flce_fwd) that allocates no device memory.
  * The paper has no counterpart to this entry point; it exists for callers
  * that cannot call cudaMalloc at the point where the loss is needed: a host

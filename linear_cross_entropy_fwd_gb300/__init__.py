@@ -33,7 +33,7 @@ TRACE_KINDS = {1: "logits_lse", 2: "combine", 3: "logits_grad", 4: "dw", 5: "dx"
 EXPORTED = ["flce_opts_init", "flce_fwd_bwd", "flce_fwd_bwd_ex", "flce_fwd",
             "flce_fwd_bwd_host", "flce_workspace_bytes", "flce_status_str",
             "flce_last_error", "flce_version", "flce_opts_sizeof", "flce_fwd_noalloc",
-            "flce_ce_fwd_bwd"]
+            "flce_ce_fwd_bwd", "flce_selftest_wait_expiry"]
 
 
 class FlceOpts(ctypes.Structure):
@@ -111,6 +111,8 @@ def load_library(path: str | None = None):
         lib.flce_fwd_noalloc.restype = i32
         lib.flce_ce_fwd_bwd.argtypes = [vp, vp, i64, i64, i64, fp, vp, po]
         lib.flce_ce_fwd_bwd.restype = i32
+        lib.flce_selftest_wait_expiry.argtypes = [i64]
+        lib.flce_selftest_wait_expiry.restype = i32
         if lib.flce_opts_sizeof() != ctypes.sizeof(FlceOpts):
             raise RuntimeError("flce_opts layout mismatch between libflce and the binding")
         _lib = lib

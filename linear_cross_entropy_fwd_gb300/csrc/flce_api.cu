@@ -872,6 +872,27 @@ int flce_ce_fwd_bwd(const void* logits, const int64_t* target, int64_t N, int64_
   return ce_entry(logits, target, N, V, ignore_index, loss, dlogits, opts);
 }
 
+int flce_selftest_wait_expiry(int64_t limit_ns) {
+  g_last_error[0] = 0;
+  if (limit_ns <= 0 || limit_ns > 2000000000) {
+    set_error("limit_ns must be in (0, 2e9]");
+    return FLCE_ERR_ARG;
+  }
+  DeviceInfo D;
+  int rc = device_info(FLCE_BF16, &D);
+  if (rc) return rc;
+  void* p = nullptr;
+  FLCE_CUDA(cudaMalloc(&p, sizeof(Scalars)));
+  Scalars* sc = static_cast<Scalars*>(p);
+  Scalars h{};
+  cudaError_t e = cudaMemset(sc, 0, sizeof(Scalars));
+  if (e == cudaSuccess) e = launch_wait_expiry(sc, static_cast<uint64_t>(limit_ns), nullptr);
+  if (e == cudaSuccess) e = cudaMemcpy(&h, sc, sizeof(Scalars), cudaMemcpyDeviceToHost);
+  cudaFree(p);
+  if (e != cudaSuccess) return cuda_fail(e, "wait-expiry self-test");
+  return status_from_bits(h.status);
+}
+
 int flce_fwd_noalloc(const void* X, const void* W, const int64_t* target, int64_t N, int64_t H,
                      int64_t V, int64_t ignore_index, int32_t dtype, float* loss_dev,
                      float* lse_out, int64_t* n_valid_dev, int32_t* status_dev, void* stream) {

@@ -88,6 +88,9 @@ constexpr int COMBINE_THREADS = 256;
 int combine_grid(int64_t N);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 
+// One block whose wait can never complete; it must expire after limit_ns.
+cudaError_t launch_wait_expiry(Scalars* sc, uint64_t limit_ns, cudaStream_t s);
+
 // Device status bits -> flce_status code in *out (one thread).
 cudaError_t launch_status_code(const Scalars* sc, int32_t* out, cudaStream_t s);
 

@@ -66,9 +66,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Returns false on
-// timeout or when another role of this CTA has already aborted.
+// timeout (limit_ns of %globaltimer) or when another role of this CTA has
+// already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
+                                          int* status,
+                                          uint64_t limit_ns = FLCE_WAIT_LIMIT_NS) {
   const uint32_t a = smem_addr(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -76,7 +78,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(a, parity)) return true;
     if ((it & 31) == 0) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > FLCE_WAIT_LIMIT_NS) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(status, FLCE_DEV_TIMEOUT);
         return false;

@@ -132,6 +132,26 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineP
   }
 }
 
+// Self-test of the bounded wait: one block waits on an mbarrier that nothing
+// will ever arrive on; the wait must expire after limit_ns, record
+// FLCE_DEV_TIMEOUT and let the kernel finish normally.
+__global__ void wait_expiry_kernel(Scalars* sc, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0, &abort_flag, &sc->status, limit_ns);
+}
+
+cudaError_t launch_wait_expiry(Scalars* sc, uint64_t limit_ns, cudaStream_t s) {
+  wait_expiry_kernel<<<1, 32, 0, s>>>(sc, limit_ns);
+  return cudaGetLastError();
+}
+
 __global__ void status_code_kernel(const Scalars* sc, int32_t* out) {
   const int32_t bits = sc->status;
   // codes of the public flce_status enum: 7 = timeout, 4 = bad target

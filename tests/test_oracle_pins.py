@@ -341,3 +341,102 @@ def test_ce_against_torch_cross_entropy():
     assert abs(r["loss"] - loss.item()) <= 1e-12 * loss.item()
     np.testing.assert_allclose(r["dS"], Sg.grad.numpy(), rtol=1e-10, atol=1e-16)
     np.testing.assert_allclose(r["dS"].sum(axis=1), 0.0, atol=1e-15)
+
+
+# --------------------------------------------- row / vocabulary subset functions
+def test_subset_functions_zero_weight_closed_forms():
+    """W = 0 pins the sampled-row and sampled-dW-row functions on their own:
+    lse = log V, row loss = log V, dX rows = 0, dW rows in closed form."""
+    N, H, V = 9, 6, 300
+    X = _rand((N, H), 71)
+    W = np.zeros((V, H))
+    t = np.array([0, 299, IGN, 5, 5, 17, IGN, 150, 2], dtype=np.int64)
+    rows = [8, 0, 2, 5]
+    r = oracle.flce_rows(X, W, t, rows, IGN)
+    np.testing.assert_allclose(r["lse"], math.log(V), rtol=1e-15)
+    np.testing.assert_allclose(r["loss_rows"], [math.log(V), math.log(V), 0.0, math.log(V)],
+                               rtol=1e-15)
+    np.testing.assert_array_equal(r["dX"], 0.0)
+    voc = [5, 0, 299, 42]
+    dw = oracle.flce_dw_rows(X, W, t, voc, IGN)
+    n = int((t != IGN).sum())
+    for k, j in enumerate(voc):
+        expect = sum((1.0 / V - (1.0 if t[i] == j else 0.0)) * X[i]
+                     for i in range(N) if t[i] != IGN) / n
+        np.testing.assert_allclose(dw[k], expect, rtol=1e-13, atol=1e-16)
+
+
+def test_subset_functions_against_torch_autograd():
+    X, W, t = make_case(20, 12, 40, "fp32", seed=72, ignore_num=20, w_std=0.7)
+    Xd = X.double().requires_grad_(True)
+    Wd = W.double().requires_grad_(True)
+    torch.nn.functional.cross_entropy(torch.nn.functional.linear(Xd, Wd), t,
+                                      ignore_index=IGN).backward()
+    rows = [19, 3, 0, 11]
+    r = oracle.flce_rows(X, W, t, rows, IGN)
+    np.testing.assert_allclose(r["dX"], Xd.grad.numpy()[rows], rtol=1e-10, atol=1e-16)
+    voc = [39, 1, 20]
+    np.testing.assert_allclose(oracle.flce_dw_rows(X, W, t, voc, IGN), Wd.grad.numpy()[voc],
+                               rtol=1e-10, atol=1e-16)
+
+
+# -------------------------------------------------------------- planted mistakes
+MUTATIONS = [
+    # (name, original text in flce_oracle.c, planted replacement)
+    ("one-hot sign in dW", "(t[i] == j ? 1.0 : 0.0);\n        g /= (double)nv;",
+     "(t[i] == j ? -1.0 : 0.0);\n        g /= (double)nv;"),
+    ("normaliser N instead of n_valid", "*loss = nv > 0 ? acc / (double)nv : 0.0;\n  if (lse)",
+     "*loss = nv > 0 ? acc / (double)N : 0.0;\n  if (lse)"),
+    ("transposed operand in dX", "dxi[h] += g * elem(W, type, j * H + h);\n        }\n      }\n      free",
+     "dxi[h] += g * elem(X, type, i * H + h);\n        }\n      }\n      free"),
+    ("dropped max shift", "for (int64_t j = 0; j < V; ++j) s += exp(srow[j] - m);",
+     "for (int64_t j = 0; j < V; ++j) s += exp(srow[j]);"),
+]
+
+
+@pytest.mark.parametrize("name,orig,planted", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_a_planted_mistake(tmp_path, name, orig, planted):
+    """Compile a copy of the oracle with one plausible slip planted (the
+    oracle itself is untouched) and check that the pins reject it."""
+    import ctypes
+    import subprocess
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "flce_oracle.c")).read()
+    assert src.count(orig) == 1, name
+    p = tmp_path / "mutant.c"
+    p.write_text(src.replace(orig, planted))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", str(so),
+                    str(p), "-lm"], check=True)
+    lib = ctypes.CDLL(str(so))
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.oracle_flce.argtypes = [vp, vp, i32, vp, i64, i64, i64, i64, vp, vp, vp, vp, vp, vp]
+    lib.oracle_flce.restype = i32
+
+    def run(X, W, t):
+        X = np.ascontiguousarray(X, dtype=np.float64)
+        W = np.ascontiguousarray(W, dtype=np.float64)
+        t = np.ascontiguousarray(t, dtype=np.int64)
+        N, H = X.shape
+        V = W.shape[0]
+        loss, nv = np.zeros(1), np.zeros(1, dtype=np.int64)
+        lse, lr = np.zeros(N), np.zeros(N)
+        dX, dW = np.zeros((N, H)), np.zeros((V, H))
+        ptr = lambda a: a.ctypes.data_as(vp)  # noqa: E731
+        lib.oracle_flce(ptr(X), ptr(W), 0, ptr(t), N, H, V, IGN, ptr(loss), ptr(nv), ptr(lse),
+                        ptr(lr), ptr(dX), ptr(dW))
+        return loss[0], dX, dW
+
+    # the torch float64 reference and the large-logit case (max shift matters)
+    Xc, Wc, tc = make_case(30, 10, 50, "fp32", seed=73, ignore_num=20, w_std=0.5)
+    Xt = Xc.double().requires_grad_(True)
+    Wt = Wc.double().requires_grad_(True)
+    ref = torch.nn.functional.cross_entropy(torch.nn.functional.linear(Xt, Wt), tc,
+                                            ignore_index=IGN)
+    ref.backward()
+    loss, dX, dW = run(Xc.double().numpy(), Wc.double().numpy(), tc.numpy())
+    big_loss, _, _ = run(Xc.double().numpy() * 100, Wc.double().numpy() * 100, tc.numpy())
+    caught = (abs(loss - ref.item()) > 1e-9 or
+              not np.allclose(dX, Xt.grad.numpy(), rtol=1e-8, atol=1e-14) or
+              not np.allclose(dW, Wt.grad.numpy(), rtol=1e-8, atol=1e-14) or
+              not np.isfinite(big_loss))
+    assert caught, f"the pins did not catch: {name}"
