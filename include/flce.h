@@ -36,7 +36,10 @@
  *     FLCE_ERR_TIMEOUT, never as a device trap.
  *   - The library needs a compute capability 10.3 device (FLCE_ERR_ARCH).
  *   - Calls are reentrant; the only process-wide state is a per-device cache
- *     of device attributes and kernel attributes.
+ *     of device attributes and kernel attributes, and one stream-ordered
+ *     memory pool per device for the scratch the library allocates itself
+ *     (it keeps freed scratch mapped for reuse until the process exits, so
+ *     it holds at most the largest scratch of the calls made so far).
  *   - Nothing throws across this boundary; every entry returns an int status.
  */
 #ifndef FLCE_H_
@@ -182,9 +185,12 @@ FLCE_API int flce_ce_fwd_bwd(const void* logits, const int64_t* target, int64_t 
 
 /*
  * End-to-end variant on HOST buffers: copies X, W and target to the device,
- * runs flce_fwd_bwd_ex, and copies loss, dX and dW back, all on opts->stream
- * (device buffers are allocated and freed stream-ordered by the library).
- * Pinned host memory gives asynchronous copies.  Always synchronous.
+ * runs the path, and copies loss, dX and dW back.  The W upload goes in
+ * pieces on a second stream with pass 1 following piece by piece, and each
+ * vocabulary chunk's dW rows are copied back as soon as they are final, while
+ * later chunks compute.  Device buffers come from the library's memory pool
+ * (stream-ordered).  Pinned host memory gives asynchronous, overlapping
+ * copies; pageable memory works but serialises them.  Always synchronous.
  */
 FLCE_API int flce_fwd_bwd_host(const void* X_host, const void* W_host, const int64_t* target_host,
                       int64_t N, int64_t H, int64_t V, int64_t ignore_index, float* loss,

@@ -364,9 +364,11 @@ def flce_ce_fwd_bwd(logits: torch.Tensor, target: torch.Tensor, ignore_index: in
 
 def flce_fwd_bwd_host(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor,
                       ignore_index: int = -100, *, dX: torch.Tensor | None = None,
-                      dW: torch.Tensor | None = None, stream=None):
-    """End to end on CPU tensors (pinned memory gives asynchronous copies):
-    the library copies the inputs in, runs, and copies loss, dX, dW out."""
+                      dW: torch.Tensor | None = None, stream=None, vocab_chunk: int = 0):
+    """End to end on CPU tensors: the library copies the inputs in, runs, and
+    copies loss, dX, dW out, overlapping the W upload with pass 1 and each
+    chunk's dW download with the later chunks (pinned memory makes the copies
+    asynchronous; pageable memory works but serialises them)."""
     lib = load_library()
     _check_inputs(X, W, target, device_needed=False)
     N, H = X.shape
@@ -376,7 +378,7 @@ def flce_fwd_bwd_host(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor,
     if dW is None:
         dW = torch.empty((V, H), dtype=torch.float32)
     loss = ctypes.c_float(0.0)
-    o = make_opts(X.dtype, stream)
+    o = make_opts(X.dtype, stream, vocab_chunk=int(vocab_chunk))
     o.dtype = _dtype_code(X)
     st = lib.flce_fwd_bwd_host(X.data_ptr(), W.data_ptr(), target.data_ptr(), N, H, V,
                                int(ignore_index), ctypes.byref(loss), dX.data_ptr(),

@@ -23,6 +23,7 @@ struct EpiRowLse {
     float* st;        // [N] target logit
     int64_t N;
     int64_t V;
+    int32_t vtile_off;  // vocabulary tile of the launch's first tile column
   };
   struct State {};
   __device__ static void init(State&) {}
@@ -30,7 +31,8 @@ struct EpiRowLse {
   __device__ static void tile(const Params& p, State&, const CUtensorMap*, uint32_t taddr,
                               int m_blk, int n_blk, int q, int lane, uint8_t*) {
     const int64_t row = static_cast<int64_t>(m_blk) * BM + 32 * q + lane;
-    const int64_t n0 = static_cast<int64_t>(n_blk) * BN;
+    const int64_t vt = static_cast<int64_t>(n_blk) + p.vtile_off;  // global vocabulary tile
+    const int64_t n0 = vt * BN;
     const int64_t rem = p.V - n0;
     const int valid_cols = rem < BN ? static_cast<int>(rem) : BN;
     const int64_t t = row < p.N ? p.target[row] : -1;
@@ -62,7 +64,7 @@ struct EpiRowLse {
         if (i == tl) st_val = __uint_as_float(r[i]);
     }
     if (row < p.N) {
-      p.partial[static_cast<int64_t>(n_blk) * p.N + row] = m + fast_log2(l);
+      p.partial[vt * p.N + row] = m + fast_log2(l);
       if (tcol >= 0) p.st[row] = st_val;
     }
   }

@@ -88,6 +88,37 @@ int device_info(int dtype, DeviceInfo* out) {
   return FLCE_OK;
 }
 
+// ------------------------------------------------------- library memory pool
+// Scratch the library allocates itself comes from one stream-ordered pool per
+// device that keeps freed memory mapped (release threshold: unlimited), so a
+// synchronous call does not re-map its scratch every time.  The pool holds at
+// most the largest scratch of the calls made so far, until the process exits.
+cudaMemPool_t g_pool[kMaxDevices] = {};
+std::mutex g_pool_mutex;
+
+int pool_alloc(void** p, size_t bytes, cudaStream_t s) {
+  int dev = 0;
+  FLCE_CUDA(cudaGetDevice(&dev));
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> lock(g_pool_mutex);
+    if (!g_pool[dev]) {
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      cudaMemPool_t np;
+      FLCE_CUDA(cudaMemPoolCreate(&np, &props));
+      uint64_t keep = UINT64_MAX;
+      FLCE_CUDA(cudaMemPoolSetAttribute(np, cudaMemPoolAttrReleaseThreshold, &keep));
+      g_pool[dev] = np;
+    }
+    pool = g_pool[dev];
+  }
+  FLCE_CUDA(cudaMallocFromPoolAsync(p, bytes, pool, s));
+  return FLCE_OK;
+}
+
 // ------------------------------------------------------------ TMA encode
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -344,10 +375,23 @@ int grid_for(int64_t tiles, int sms) {
   return static_cast<int>(tiles < sms ? tiles : sms);
 }
 
+// Copies of the host-buffer entry that overlap the path: W arrives in pieces
+// on a copy stream (pass 1 runs piece by piece as they land), and each chunk's
+// dW rows go back to the host as soon as their GEMM is done.
+struct HostOverlap {
+  cudaStream_t copy;
+  int32_t n_w_pieces;
+  int64_t w_piece_tiles;        // vocabulary tiles of BN rows per piece
+  const cudaEvent_t* w_ready;   // [n_w_pieces], recorded on `copy`
+  float* dW_host;
+  const cudaEvent_t* chunk_done;  // [num_chunks]
+  cudaEvent_t copies_done;
+};
+
 // The whole path on device pointers.  `ws` holds at least plan.total bytes.
 int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
              const int64_t* target, int64_t ignore_index, void* dX, float* dW, uint8_t* ws,
-             const flce_opts& o, cudaStream_t s) {
+             const flce_opts& o, cudaStream_t s, const HostOverlap* ov = nullptr) {
   const int64_t N = P.N, H = P.H, V = P.V;
   const int elt = P.elt;
   const bool bf16 = (P.dtype == FLCE_BF16);
@@ -372,16 +416,23 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
     CUtensorMap mX, mW;
     if ((rc = make_map(&mX, X, dt, elt, H, N, H * elt, KE, BM, "X (K-major)"))) return rc;
     if ((rc = make_map(&mW, W, dt, elt, H, V, H * elt, KE, BR, "W (K-major)"))) return rc;
-    GemmGrid g{};
-    g.num_m_blk = static_cast<int32_t>((N + MB - 1) / MB);
-    g.num_n_blk = static_cast<int32_t>(P.num_vblk);
-    g.num_k_blk = static_cast<int32_t>((H + KE - 1) / KE);
-    g.status = &sc->status;
-    RowLseParams rp{target, partial, st, N, V};
-    const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, units);
-    FLCE_CUDA(bf16 ? launch_logits_lse_bf16(mX, mW, g, rp, grid, s)
-                   : launch_logits_lse_fp32(mX, mW, g, rp, grid, s));
-    if ((rc = tr.after(FLCE_TRACE_LOGITS_LSE))) return rc;
+    // one launch over the whole vocabulary, or one per uploaded piece of W
+    const int64_t piece = ov ? ov->w_piece_tiles : P.num_vblk;
+    for (int64_t t0 = 0, pi = 0; t0 < P.num_vblk; t0 += piece, ++pi) {
+      const int64_t nt = (P.num_vblk - t0) < piece ? (P.num_vblk - t0) : piece;
+      if (ov) FLCE_CUDA(cudaStreamWaitEvent(s, ov->w_ready[pi], 0));
+      GemmGrid g{};
+      g.num_m_blk = static_cast<int32_t>((N + MB - 1) / MB);
+      g.num_n_blk = static_cast<int32_t>(nt);
+      g.num_k_blk = static_cast<int32_t>((H + KE - 1) / KE);
+      g.b_mn_off = static_cast<int32_t>(t0 * BN);
+      g.status = &sc->status;
+      RowLseParams rp{target, partial, st, N, V, static_cast<int32_t>(t0)};
+      const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, units);
+      FLCE_CUDA(bf16 ? launch_logits_lse_bf16(mX, mW, g, rp, grid, s)
+                     : launch_logits_lse_fp32(mX, mW, g, rp, grid, s));
+      if ((rc = tr.after(FLCE_TRACE_LOGITS_LSE))) return rc;
+    }
   }
   CombineParams cp{};
   cp.partial = partial;
@@ -478,6 +529,13 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
           FLCE_CUDA(bf16 ? launch_dw_bf16(mA4, mB4, mdW, g, sp, grid, s)
                          : launch_dw_fp32(mA4, mB4, mdW, g, sp, grid, s));
           if ((rc = tr.after(FLCE_TRACE_DW))) return rc;
+          if (ov) {  // these dW rows are final: send them to the host now
+            FLCE_CUDA(cudaEventRecord(ov->chunk_done[c], s));
+            FLCE_CUDA(cudaStreamWaitEvent(ov->copy, ov->chunk_done[c], 0));
+            FLCE_CUDA(cudaMemcpyAsync(ov->dW_host + c0 * H, dW + c0 * H,
+                                      static_cast<size_t>(vc) * H * 4, cudaMemcpyDeviceToHost,
+                                      ov->copy));
+          }
         }
         // dX_acc (+)= G_c W[c0 : c0+vc]
         {
@@ -501,6 +559,10 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
       }
     }
   }
+  if (ov && N > 0) {  // the compute stream continues only once dW is home
+    FLCE_CUDA(cudaEventRecord(ov->copies_done, ov->copy));
+    FLCE_CUDA(cudaStreamWaitEvent(s, ov->copies_done, 0));
+  }
   if (o.status_dev) FLCE_CUDA(launch_status_code(sc, o.status_dev, s));
   tr.finish();
   return FLCE_OK;
@@ -520,7 +582,7 @@ int status_from_bits(int32_t bits) {
 
 int entry(const void* X, const void* W, const int64_t* target, int64_t N, int64_t H, int64_t V,
           int64_t ignore_index, float* loss_host, void* dX, float* dW, const flce_opts* opts_in,
-          bool grads) {
+          bool grads, const HostOverlap* ov = nullptr) {
   g_last_error[0] = 0;
   flce_opts o;
   flce_opts_init(&o);
@@ -561,11 +623,11 @@ int entry(const void* X, const void* W, const int64_t* target, int64_t N, int64_
   bool owned = false;
   if (!ws) {
     void* p = nullptr;
-    FLCE_CUDA(cudaMallocAsync(&p, P.total, s));
+    if ((rc = pool_alloc(&p, P.total, s))) return rc;
     ws = static_cast<uint8_t*>(p);
     owned = true;
   }
-  rc = run_path(P, D, X, W, target, ignore_index, dX, dW, ws, o, s);
+  rc = run_path(P, D, X, W, target, ignore_index, dX, dW, ws, o, s, ov);
   Scalars host_sc{};
   if (rc == FLCE_OK && sync) {
     cudaError_t e = cudaMemcpyAsync(&host_sc, ws + P.off_sc, sizeof(Scalars),
@@ -635,7 +697,7 @@ int ce_entry(const void* logits, const int64_t* target, int64_t N, int64_t V,
   bool owned = false;
   if (!ws) {
     void* pws = nullptr;
-    FLCE_CUDA(cudaMallocAsync(&pws, total, s));
+    if ((rc = pool_alloc(&pws, total, s))) return rc;
     ws = static_cast<uint8_t*>(pws);
     owned = true;
   }
@@ -799,41 +861,97 @@ int flce_fwd_bwd_host(const void* X_host, const void* W_host, const int64_t* tar
     set_error("null host pointer");
     return FLCE_ERR_ARG;
   }
-  if (N < 0 || H <= 0 || V <= 0) {
-    set_error("bad sizes");
+  if (N < 0 || H <= 0 || V <= 0 || (o.dtype != FLCE_BF16 && o.dtype != FLCE_FP32)) {
+    set_error("bad sizes or dtype");
     return FLCE_ERR_ARG;
   }
+  Plan P;
+  int rc = make_plan(&P, N, H, V, true, o, o.workspace_budget);
+  if (rc) return rc;
   const size_t elt = (o.dtype == FLCE_FP32) ? 4 : 2;
   const size_t bx = static_cast<size_t>(N) * H * elt, bw = static_cast<size_t>(V) * H * elt,
                bt = static_cast<size_t>(N) * 8, bdw = static_cast<size_t>(V) * H * 4;
   cudaStream_t s = static_cast<cudaStream_t>(o.stream);
   const size_t ox = 0, ow = align_up(ox + bx, 256), ot = align_up(ow + bw, 256),
                odx = align_up(ot + bt, 256), odw = align_up(odx + bx, 256),
-               total = align_up(odw + bdw, 256);
+               osc = align_up(odw + bdw, 256), total = osc + 256;
+  // W goes up in pieces of whole vocabulary tiles, pass 1 following them
+  constexpr int kPieces = 8;
+  const int64_t piece_tiles = (P.num_vblk + kPieces - 1) / kPieces;
+  const int n_pieces = static_cast<int>((P.num_vblk + piece_tiles - 1) / piece_tiles);
+  const int n_chunks = static_cast<int>(P.num_chunks);
   void* buf = nullptr;
-  FLCE_CUDA(cudaMallocAsync(&buf, total, s));
+  if ((rc = pool_alloc(&buf, total, s))) return rc;
   uint8_t* b = static_cast<uint8_t*>(buf);
-  int rc = FLCE_OK;
-  cudaError_t e = cudaSuccess;
-  if (bx) e = cudaMemcpyAsync(b + ox, X_host, bx, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(b + ow, W_host, bw, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess && bt) e = cudaMemcpyAsync(b + ot, target_host, bt, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemcpyAsync(H2D)");
-  if (rc == FLCE_OK) {
-    o.sync = 1;
-    rc = entry(b + ox, b + ow, reinterpret_cast<const int64_t*>(b + ot), N, H, V, ignore_index,
-               loss, b + odx, reinterpret_cast<float*>(b + odw), &o, true);
+  float* loss_dev = reinterpret_cast<float*>(b + osc);
+  int32_t* status_dev = reinterpret_cast<int32_t*>(b + osc + 16);
+  cudaStream_t cs = nullptr;
+  const int n_events = n_pieces + n_chunks + 2;
+  cudaEvent_t* ev = new cudaEvent_t[n_events]();
+  cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+  for (int i = 0; e == cudaSuccess && i < n_events; ++i)
+    e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+  cudaEvent_t* w_ready = ev;
+  cudaEvent_t* chunk_done = ev + n_pieces;
+  cudaEvent_t alloc_ready = ev[n_events - 2], copies_done = ev[n_events - 1];
+  if (e == cudaSuccess) e = cudaEventRecord(alloc_ready, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, alloc_ready, 0);
+  if (e == cudaSuccess && bx) e = cudaMemcpyAsync(b + ox, X_host, bx, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && bt)
+    e = cudaMemcpyAsync(b + ot, target_host, bt, cudaMemcpyHostToDevice, s);
+  for (int p = 0; e == cudaSuccess && p < n_pieces; ++p) {
+    const int64_t r0 = p * piece_tiles * BN;
+    const int64_t r1 = (r0 + piece_tiles * BN) < V ? (r0 + piece_tiles * BN) : V;
+    const size_t off = static_cast<size_t>(r0) * H * elt, len = static_cast<size_t>(r1 - r0) * H * elt;
+    e = cudaMemcpyAsync(b + ow + off, static_cast<const uint8_t*>(W_host) + off, len,
+                        cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess) e = cudaEventRecord(w_ready[p], cs);
   }
+  if (e != cudaSuccess) rc = cuda_fail(e, "host-buffer staging");
   if (rc == FLCE_OK) {
-    if (bx) e = cudaMemcpyAsync(dX_host, b + odx, bx, cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dW_host, b + odw, bdw, cudaMemcpyDeviceToHost, s);
+    HostOverlap ov{cs, n_pieces, piece_tiles, w_ready, dW_host, chunk_done, copies_done};
+    if (N == 0) {  // no pass 1 waits on the pieces: order the stream after them
+      e = cudaEventRecord(copies_done, cs);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(s, copies_done, 0);
+      if (e != cudaSuccess) rc = cuda_fail(e, "host-buffer staging");
+    }
+    flce_opts io = o;
+    io.sync = 0;
+    io.loss_dev = loss_dev;
+    io.status_dev = status_dev;
+    if (rc == FLCE_OK)
+      rc = entry(b + ox, b + ow, reinterpret_cast<const int64_t*>(b + ot), N, H, V, ignore_index,
+                 nullptr, b + odx, reinterpret_cast<float*>(b + odw), &io, true,
+                 N > 0 ? &ov : nullptr);
+  }
+  float h_loss = 0.f;
+  int32_t h_status = 0;
+  if (rc == FLCE_OK) {
+    e = cudaSuccess;
+    if (N == 0) e = cudaMemcpyAsync(dW_host, b + odw, bdw, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && bx) e = cudaMemcpyAsync(dX_host, b + odx, bx, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&h_loss, loss_dev, 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&h_status, status_dev, 4, cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemcpyAsync(D2H)");
   }
   e = cudaFreeAsync(buf, s);
   if (e != cudaSuccess && rc == FLCE_OK) rc = cuda_fail(e, "cudaFreeAsync");
   e = cudaStreamSynchronize(s);
   if (e != cudaSuccess && rc == FLCE_OK) rc = cuda_fail(e, "cudaStreamSynchronize");
-  return rc;
+  if (cs) {
+    cudaStreamSynchronize(cs);
+    cudaStreamDestroy(cs);
+  }
+  for (int i = 0; i < n_events; ++i)
+    if (ev[i]) cudaEventDestroy(ev[i]);
+  delete[] ev;
+  if (rc != FLCE_OK) return rc;
+  if (h_status == FLCE_ERR_TIMEOUT || h_status == FLCE_ERR_TARGET) {
+    set_error("%s", flce_status_str(h_status));
+    return h_status;
+  }
+  *loss = h_loss;
+  return FLCE_OK;
 }
 
 size_t flce_workspace_bytes(int64_t N, int64_t H, int64_t V, int with_grads,

@@ -80,7 +80,7 @@ struct Kernels {
 
   static cudaError_t run_lse(const CUtensorMap& A, const CUtensorMap& B, const GemmGrid& g,
                              const RowLseParams& p, int units, cudaStream_t s) {
-    EpiRowLse::Params ep{p.target, p.partial, p.st, p.N, p.V};
+    EpiRowLse::Params ep{p.target, p.partial, p.st, p.N, p.V, p.vtile_off};
     return launch(lse, A, B, A, g, ep, units, s);
   }
 

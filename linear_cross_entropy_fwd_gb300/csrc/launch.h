@@ -13,6 +13,7 @@ struct RowLseParams {
   float* st;
   int64_t N;
   int64_t V;
+  int32_t vtile_off;  // vocabulary tile of the launch's first tile column
 };
 
 struct GradLogitsParams {

@@ -160,6 +160,25 @@ def test_simple_and_host_entry_points(cuda_lib):
     assert torch.equal(dX_h, dX.cpu()) and torch.equal(dW_h, dW.cpu())
 
 
+@pytest.mark.parametrize("N,H,V,dtype,vc,pinned", [
+    (700, 256, 9000, "bf16", 2048, True),   # 5 chunks, 8 W pieces, dW rows sent per chunk
+    (300, 128, 3000, "bf16", 0, False),     # pageable host memory
+    (100, 64, 2000, "fp32", 512, True),     # fp32 (tf32) path
+])
+def test_host_entry_overlapped_copies(cuda_lib, N, H, V, dtype, vc, pinned):
+    X, W, t = make_case(N, H, V, dtype, seed=N + H, ignore_num=10,
+                        w_std=0.088 if dtype == "fp32" else 0.02)
+    dev = cuda_lib.flce_fwd_bwd_ex(*_gpu(X, W, t), IGN, sync=True, vocab_chunk=vc)
+    if pinned:
+        X, W, t = X.pin_memory(), W.pin_memory(), t.pin_memory()
+    loss, dX, dW = cuda_lib.flce_fwd_bwd_host(X, W, t, IGN, vocab_chunk=vc)
+    assert loss == dev[0].item()
+    assert torch.equal(dX, dev[2].cpu()) and torch.equal(dW, dev[3].cpu())
+    ref = oracle.flce(X, W, t, IGN)
+    assert_loss(loss, ref["loss"])
+    assert_grad(dW.numpy(), ref["dW"], "dW")
+
+
 def test_deterministic(cuda_lib):
     X, W, t = make_case(600, 256, 4000, "bf16", seed=18, ignore_num=5)
     Xd, Wd, td = _gpu(X, W, t)
