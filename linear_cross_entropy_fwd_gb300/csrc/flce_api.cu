@@ -209,6 +209,10 @@ size_t fixed_bytes(Plan& p) {
 }
 
 constexpr int64_t kMinChunk = 2048;
+// The default budget never goes below this: where one sixteenth of the
+// logits is smaller, the fixed part alone (the fp32 dX accumulator) can
+// exceed it and the chunk loop would be all launch overhead.
+constexpr size_t kBudgetFloor = size_t{64} << 20;
 // Scheduling units the planner assumes (GB300: 152 SMs = 76 CTA pairs), so
 // that a plan, and flce_workspace_bytes(), do not depend on which device
 // (if any) is current when it is made.
@@ -245,7 +249,8 @@ int64_t chunk_loop_cost(int64_t N, int64_t H, int64_t V, int64_t Vc, int elt, bo
   return cost;
 }
 
-// budget: bytes the plan may use (0 = N*V*4/16).  Returns FLCE_OK or an error.
+// budget: bytes the plan may use (0 = the larger of N*V*4/16 and kBudgetFloor).
+// Returns FLCE_OK or an error.
 int make_plan(Plan* out, int64_t N, int64_t H, int64_t V, bool grads, const flce_opts& o,
               size_t budget) {
   Plan p;
@@ -269,7 +274,10 @@ int make_plan(Plan* out, int64_t N, int64_t H, int64_t V, bool grads, const flce
       }
       Vc = o.vocab_chunk;
     } else {
-      if (budget == 0) budget = static_cast<size_t>(N) * static_cast<size_t>(V) * 4 / 16;
+      if (budget == 0) {
+        budget = static_cast<size_t>(N) * static_cast<size_t>(V) * 4 / 16;
+        if (budget < kBudgetFloor) budget = kBudgetFloor;
+      }
       size_t per_col = static_cast<size_t>(N) * p.elt;  // G chunk column
       if (p.dtype == FLCE_FP32)                            // + G^T and W^T columns
         per_col += static_cast<size_t>(p.Np) * 4 + static_cast<size_t>(H) * 4;
