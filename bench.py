@@ -200,7 +200,7 @@ def run_reference(args, workload):
 
 
 def run_ce_logits(args, w):
-    """Cross-entropy on materialised bf16 logits [N, V] (loss + gradient into
+    """Cross-entropy on materialised logits [N, V], bf16 or fp32 (loss + gradient into
     a separate buffer).  HBM-bound: the roofline is bytes moved per launch of
     the row kernel (one read and one write of the logits) over its time."""
     import torch
@@ -214,6 +214,8 @@ def run_ce_logits(args, w):
     peaks, peak_src = load_peaks()
     X, W, t = make_inputs(w)
     S = (X.to(dev) @ W.to(dev).t()).contiguous()  # input staging (cuBLAS), not timed
+    if args.ce_dtype == "fp32":
+        S = S.float()
     td = t.to(dev)
     dS = torch.empty_like(S)
     del X, W
@@ -247,7 +249,8 @@ def run_ce_logits(args, w):
         "metric": "tokens/s, cross-entropy on materialised logits (loss + gradient), 1 GB300",
         "value": w.N / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (logits = X W^T of the workload)",
+        "vs_baseline": None, "dtype": args.ce_dtype,
+        "data": "synthetic (logits = X W^T of the workload)",
         "config": workload_config(w, 1),
         "roofline": {"bound": "hbm", "kernel": "ce_rows", "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm,
@@ -272,6 +275,8 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="flce", choices=["flce", "reference"])
+    ap.add_argument("--ce-dtype", default="bf16", choices=["bf16", "fp32"],
+                    help="element type of the logits for --op ce_logits")
     ap.add_argument("--op", default="flce", choices=["flce", "ce_logits"],
                     help="flce: the fused path (default); ce_logits: cross-entropy on "
                          "logits already in HBM (logits = X W^T of the workload, bf16)")

@@ -24,15 +24,18 @@ def _targets(N, V, seed, ignore_num):
 
 
 @pytest.mark.parametrize("N,V,dtype,ign", [
-    (4, 256, "fp32", 0),
-    (300, 1000, "bf16", 10),        # vector path (1000 * 2 % 16 == 0)
-    (257, 777, "bf16", 5),          # scalar path (777 * 2 % 16 != 0)
-    (129, 32000, "bf16", 20),
-    (64, 5003, "fp32", 0),          # scalar path, fp32
-    (33, 128256, "bf16", 3),        # a Llama-3-sized row: cluster of 4 CTAs per row
-    (40, 60000, "bf16", 10),        # cluster of 2
-    (17, 128256, "fp32", 0),        # fp32 row of 513 KB: cluster of 8
-    (301, 4096, "fp32", 30),        # many rows per cluster (double-buffered slices)
+    # 16-byte vector path (rows 16-byte aligned, V * elt % 16 == 0)
+    (4, 256, "fp32", 0),            # rows shorter than one pass of the CTA
+    (300, 1000, "bf16", 10),        # vector tail only
+    (129, 32000, "bf16", 20),       # unrolled body and tail
+    (33, 128256, "bf16", 3),        # a Llama-3-sized row
+    (40, 60000, "bf16", 10),
+    (17, 128256, "fp32", 0),        # fp32 row of 513 KB
+    (301, 4096, "fp32", 30),        # 2 rows on most CTAs
+    (700, 20000, "bf16", 5),        # several rows per CTA
+    # scalar path (a row is not a multiple of 16 bytes)
+    (257, 777, "bf16", 5),
+    (64, 5003, "fp32", 0),
 ])
 def test_ce_matches_oracle(cuda_lib, N, V, dtype, ign):
     S = _logits(N, V, dtype, seed=N + V)
@@ -62,6 +65,18 @@ def test_ce_in_place_and_loss_only(cuda_lib):
     loss2, _, none = cuda_lib.flce_ce_fwd_bwd(S2, t.to(DEV), IGN, sync=True, grad=False)
     assert none is None and loss2.item() == loss.item()
     assert torch.equal(S2.cpu(), S)  # the logits are untouched without a gradient
+
+
+def test_ce_in_place_long_rows(cuda_lib):
+    """In place with long rows and two rows on some CTAs: each element is
+    read twice (statistics, then gradient) and then overwritten."""
+    S = _logits(180, 50000, "bf16", seed=67)
+    t = _targets(180, 50000, seed=68, ignore_num=7)
+    ref = oracle.ce(S, t, IGN)
+    buf = S.to(DEV)
+    loss, _, _ = cuda_lib.flce_ce_fwd_bwd(buf, t.to(DEV), IGN, sync=True, inplace=True)
+    assert_loss(loss.item(), ref["loss"])
+    assert_grad(buf.float().cpu().numpy(), ref["dS"], "in-place dS")
 
 
 def test_ce_matches_fused_path_on_the_same_logits(cuda_lib):
