@@ -40,6 +40,11 @@
  *     memory pool per device for the scratch the library allocates itself
  *     (it keeps freed scratch mapped for reuse until the process exits, so
  *     it holds at most the largest scratch of the calls made so far).
+ *   - An asynchronous call (opts->sync == 0, host loss NULL, no trace events)
+ *     makes only stream-ordered CUDA calls: scratch allocation and release,
+ *     memsets and kernel launches.  It can therefore be captured into a CUDA
+ *     graph (after one call outside the capture has set up the per-device
+ *     state), and replays reproduce an eager call bit for bit.
  *   - Nothing throws across this boundary; every entry returns an int status.
  */
 #ifndef FLCE_H_
