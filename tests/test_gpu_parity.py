@@ -80,6 +80,30 @@ def test_targets_in_last_partial_tile(cuda_lib):
     _check_full(cuda_lib, X, W, t2, vocab_chunk=256)
 
 
+def test_single_word_vocabulary(cuda_lib):
+    """V = 1: the softmax is exactly 1, so the exact loss and gradients are 0.
+    The kernels form 2^(S log2 e - lse2) with lse2 rounded in fp32, so they
+    may leave a residual of a few ulp of the unit-size terms."""
+    X, W, t = make_case(70, 64, 1, "bf16", seed=17)
+    t[:] = 0
+    loss, nval, dX, dW = cuda_lib.flce_fwd_bwd_ex(*_gpu(X, W, t), IGN, sync=True)
+    assert int(nval.item()) == 70
+    assert abs(loss.item()) <= 1e-4
+    assert dX.float().abs().max().item() <= 1e-5 * W.float().abs().max().item()
+    assert dW.abs().max().item() <= 1e-5 * X.float().abs().max().item()
+
+
+@pytest.mark.parametrize("N,H,V,vc", [
+    (90, 64, 2, 0),          # two words: the oracle's loss is the softplus closed form
+    (50, 8, 300, 0),         # the narrowest bf16 rows (16 bytes): one K block, mostly fill
+    (32, 256, 256000, 0),    # a 256k vocabulary in one chunk (1000 vocabulary tiles)
+    (32, 256, 256000, 65536),  # the same in four chunks, ragged last one
+])
+def test_vocabulary_and_width_extremes(cuda_lib, N, H, V, vc):
+    X, W, t = make_case(N, H, V, "bf16", seed=N + H, ignore_num=3, w_std=0.3)
+    _check_full(cuda_lib, X, W, t, vocab_chunk=vc)
+
+
 def test_all_ignored_gives_zero(cuda_lib):
     X, W, _ = make_case(64, 64, 512, "bf16", seed=12)
     t = torch.full((64,), IGN, dtype=torch.int64)
