@@ -16,48 +16,73 @@ namespace flce {
 
 constexpr float kLn2 = 0.69314718055994531f;
 
+// Online log2-domain sum: (m, l) holds max u and sum 2^(u - m).
+__device__ __forceinline__ void online_add(float& m, float& l, float u) {
+  // u in the log2 domain (logit * log2 e)
+  if (u > m) {
+    l = l * fast_exp2(m - u) + 1.f;
+    m = u;
+  } else {
+    l += fast_exp2(u - m);
+  }
+}
+
+__device__ __forceinline__ void online_merge(float& m, float& l, float m2, float l2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) return;
+  l = (m == -INFINITY ? 0.f : l * fast_exp2(m - M)) + (m2 == -INFINITY ? 0.f : l2 * fast_exp2(m2 - M));
+  m = M;
+}
+
+// Rows per combine block: one per lane; the block's warps split the row's
+// vocabulary tiles (warp w takes tiles w, w + COMBINE_SPLIT, ...), so every
+// warp load reads 32 consecutive rows of one tile (128 contiguous bytes).
+constexpr int COMBINE_ROWS = 32;
+constexpr int COMBINE_SPLIT = COMBINE_THREADS / 32;
+
 int combine_grid(int64_t N) {
-  const int64_t b = (N + COMBINE_THREADS - 1) / COMBINE_THREADS;
+  const int64_t b = (N + COMBINE_ROWS - 1) / COMBINE_ROWS;
   return b < 1 ? 1 : static_cast<int>(b);
 }
 
-// One thread per row.  lse2_i = M + log2(sum_b 2^(p_b - M)), M = max_b p_b,
-// over the row's per-tile statistics p_b = m_b + log2(l_b) (pass 1).  The
-// row loss is lse_i - S_{i,t_i} with lse_i = lse2_i ln 2.  Sums: per block a
-// fixed shuffle tree in double, then the last block to finish adds the block
-// sums in index order, so the result does not depend on scheduling.
+// lse2_i = M + log2(sum_b 2^(p_b - M)), M = max_b p_b, over the row's per-tile
+// statistics p_b = m_b + log2(l_b) (pass 1).  Each warp folds its share of
+// the tiles with an online max/sum; the shares are merged in warp order.
+// The row loss is lse_i - S_{i,t_i} with lse_i = lse2_i ln 2.  Sums: per
+// block a fixed shuffle tree in double, then the last block to finish adds
+// the block sums in index order, so the result does not depend on scheduling.
 __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineParams p) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * COMBINE_THREADS + threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * COMBINE_ROWS + lane;
+  __shared__ float s_m[COMBINE_SPLIT][COMBINE_ROWS], s_l[COMBINE_SPLIT][COMBINE_ROWS];
+  __shared__ bool s_last;
+  {
+    float m = -INFINITY, l = 0.f;
+    if (i < p.N) {
+      const float* col = p.partial + i;
+      int b = warp;
+      for (; b + 3 * COMBINE_SPLIT < p.num_vblk; b += 4 * COMBINE_SPLIT) {
+        float v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          v[k] = __ldg(col + static_cast<int64_t>(b + k * COMBINE_SPLIT) * p.N);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) online_add(m, l, v[k]);
+      }
+      for (; b < p.num_vblk; b += COMBINE_SPLIT)
+        online_add(m, l, __ldg(col + static_cast<int64_t>(b) * p.N));
+    }
+    s_m[warp][lane] = m;
+    s_l[warp][lane] = l;
+  }
+  __syncthreads();
   double row_loss = 0.0;
   int cnt = 0;
-  if (i < p.N) {
-    float m = -INFINITY, s = 0.f;
-    const float* col = p.partial + i;
-    int b = 0;
-    for (; b + 4 <= p.num_vblk; b += 4) {
-      float v[4];
+  if (warp == 0 && i < p.N) {
+    float m = s_m[0][lane], l = s_l[0][lane];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = __ldg(col + static_cast<int64_t>(b + k) * p.N);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (v[k] > m) {
-          s = s * fast_exp2(m - v[k]) + 1.f;
-          m = v[k];
-        } else {
-          s += fast_exp2(v[k] - m);
-        }
-      }
-    }
-    for (; b < p.num_vblk; ++b) {
-      const float v = __ldg(col + static_cast<int64_t>(b) * p.N);
-      if (v > m) {
-        s = s * fast_exp2(m - v) + 1.f;
-        m = v;
-      } else {
-        s += fast_exp2(v - m);
-      }
-    }
-    const float lse2 = m + fast_log2(s);
+    for (int w = 1; w < COMBINE_SPLIT; ++w) online_merge(m, l, s_m[w][lane], s_l[w][lane]);
+    const float lse2 = m + fast_log2(l);
     p.lse2[i] = lse2;
     const float lse = lse2 * kLn2;
     if (p.lse_out) p.lse_out[i] = lse;
@@ -74,33 +99,20 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineP
     if (p.loss_rows_out) p.loss_rows_out[i] = lr;
     row_loss = lr;
   }
-  // block reduction (fixed order)
+  // block reduction (fixed order): warp 0 holds the block's rows
+  if (warp == 0) {
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    row_loss += __shfl_xor_sync(0xffffffffu, row_loss, off);
-    cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
-  }
-  __shared__ double s_loss[COMBINE_THREADS / 32];
-  __shared__ int s_cnt[COMBINE_THREADS / 32];
-  __shared__ bool s_last;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
-    s_loss[warp] = row_loss;
-    s_cnt[warp] = cnt;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double a = 0.0;
-    int64_t c = 0;
-    for (int w = 0; w < COMBINE_THREADS / 32; ++w) {
-      a += s_loss[w];
-      c += s_cnt[w];
+    for (int off = 16; off > 0; off >>= 1) {
+      row_loss += __shfl_xor_sync(0xffffffffu, row_loss, off);
+      cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
     }
-    p.blk_loss[blockIdx.x] = a;
-    p.blk_cnt[blockIdx.x] = c;
-    __threadfence();
-    const unsigned ticket = atomicAdd(&p.sc->ticket, 1u);
-    s_last = (ticket == gridDim.x - 1);
+    if (lane == 0) {
+      p.blk_loss[blockIdx.x] = row_loss;
+      p.blk_cnt[blockIdx.x] = cnt;
+      __threadfence();
+      const unsigned ticket = atomicAdd(&p.sc->ticket, 1u);
+      s_last = (ticket == gridDim.x - 1);
+    }
   }
   __syncthreads();
   if (!s_last || warp != 0) return;
@@ -309,23 +321,6 @@ struct CeVec<4> {  // 4 fp32 per 16-byte access
   }
   __device__ static void store1(void* p, int64_t i, float v) { static_cast<float*>(p)[i] = v; }
 };
-
-__device__ __forceinline__ void online_add(float& m, float& l, float u) {
-  // u in the log2 domain (logit * log2 e)
-  if (u > m) {
-    l = l * fast_exp2(m - u) + 1.f;
-    m = u;
-  } else {
-    l += fast_exp2(u - m);
-  }
-}
-
-__device__ __forceinline__ void online_merge(float& m, float& l, float m2, float l2) {
-  const float M = fmaxf(m, m2);
-  if (M == -INFINITY) return;
-  l = (m == -INFINITY ? 0.f : l * fast_exp2(m - M)) + (m2 == -INFINITY ? 0.f : l2 * fast_exp2(m2 - M));
-  m = M;
-}
 
 // The row kernel keeps several rows in flight per SM (one per CTA) so that
 // enough 16-byte loads are outstanding to run near the HBM copy rate.  Its
