@@ -104,6 +104,16 @@ def test_vocabulary_and_width_extremes(cuda_lib, N, H, V, vc):
     _check_full(cuda_lib, X, W, t, vocab_chunk=vc)
 
 
+def test_launch_sequence(cuda_lib):
+    """Per-launch trace of a three-chunk call: pass 1, combine, then pass 2,
+    dW and dX per chunk, then the bf16 conversion of dX."""
+    X, W, t = make_case(300, 128, 2000, "bf16", seed=18, ignore_num=10)
+    tr = cuda_lib.Trace(capacity=16)
+    cuda_lib.flce_fwd_bwd_ex(*_gpu(X, W, t), IGN, sync=True, vocab_chunk=768, trace=tr)
+    kinds = [k for k, _ in tr.launches()]
+    assert kinds == ["logits_lse", "combine"] + ["logits_grad", "dw", "dx"] * 3 + ["convert"]
+
+
 def test_all_ignored_gives_zero(cuda_lib):
     X, W, _ = make_case(64, 64, 512, "bf16", seed=12)
     t = torch.full((64,), IGN, dtype=torch.int64)
