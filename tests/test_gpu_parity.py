@@ -65,6 +65,28 @@ def test_fwd_bwd_matches_oracle(cuda_lib, N, H, V, dtype, ign, vc):
         assert info["vocab_chunk"] == vc
 
 
+def _random_cases(n=24, seed=20261202):
+    """Seeded shapes: every N, H and V tail, ignored rows, explicit chunk
+    widths (0 = planner) and both element types (fp32 runs on tf32)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for k in range(n):
+        dtype = "fp32" if k % 4 == 3 else "bf16"
+        N = int(rng.integers(1, 900))
+        H = int(rng.integers(1, 48)) * (4 if dtype == "fp32" else 8)  # 16-byte rows
+        V = int(rng.integers(2, 6000))
+        ign = min(int(rng.integers(0, 40)), N)
+        vc = int(rng.choice([0, 256, 512, 1280, 2048]))
+        out.append((N, H, V, dtype, ign, vc))
+    return out
+
+
+@pytest.mark.parametrize("N,H,V,dtype,ign,vc", _random_cases())
+def test_randomized_shapes(cuda_lib, N, H, V, dtype, ign, vc):
+    X, W, t = make_case(N, H, V, dtype, seed=7 * N + V, ignore_num=ign, w_std=0.05)
+    _check_full(cuda_lib, X, W, t, vocab_chunk=vc)
+
+
 def test_large_logits_range(cuda_lib):
     """W scaled up so logits span about +-40: the max-shifted sums must hold."""
     X, W, t = make_case(200, 256, 1500, "bf16", seed=9, ignore_num=5, w_std=0.15)
