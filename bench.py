@@ -262,6 +262,68 @@ def run_ce_logits(args, w):
     return 0
 
 
+def run_fwd(args, w):
+    """The loss-only evaluation path (flce_fwd): pass 1 and the combine, on
+    inputs resident in HBM.  Useful work 2*N*H*V FLOP per call; the roofline
+    is pass 1's executed FLOPs per launch over its mean event time."""
+    import torch
+
+    import linear_cross_entropy_fwd_gb300 as flce
+    from flce_synth import make_inputs
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    flce.load_library()
+    peaks, peak_src = load_peaks()
+    X, W, t = make_inputs(w)
+    Xd, Wd, td = X.to(dev), W.to(dev), t.to(dev)
+    N, H, V = w.N, w.H, w.V
+    for _ in range(max(args.warmup, 1)):
+        flce.flce_fwd(Xd, Wd, td, w.ignore_index)
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(None)
+    sampler.start()
+    time.sleep(0.3)
+    e0.record(stream)
+    for _ in range(args.steps):
+        flce.flce_fwd(Xd, Wd, td, w.ignore_index)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    traces = [flce.Trace(capacity=8) for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for k in range(args.steps):
+        flce.flce_fwd(Xd, Wd, td, w.ignore_index, trace=traces[k])
+    torch.cuda.synchronize(dev)
+    lse_ms = [t_ms for tr in traces for kind, t_ms in tr.launches() if kind == "logits_lse"]
+    lse_avg = sum(lse_ms) / len(lse_ms)
+    flops = 2.0 * N * H * V
+    peak_sust = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    peak_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    achieved = flops / (lse_avg * 1e-3) / 1e12
+    useful = flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": "tokens/s, fused linear CE loss only (flce_fwd), 1 GB300",
+        "value": N / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64 + Box-Muller inputs, random-init LM head)",
+        "config": workload_config(w, 1),
+        "useful_tflops": useful, "frac_of_bf16_peak": useful / peak_burst,
+        "roofline": {"bound": "tensor", "kernel": "logits_lse", "achieved": achieved,
+                     "peak": peak_sust, "unit": "TFLOP/s", "frac": achieved / peak_sust,
+                     "peak_kind": f"bf16 dense, sustained ({peak_src})",
+                     "frac_of_burst": achieved / peak_burst, "flops_per_launch": flops,
+                     "traffic": recorded_traffic("logits_lse", w.name)},
+        "gpu_launches": 3 * args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def workload_config(w, n_gpus):
     return {"workload": w.name, "N": w.N, "H": w.H, "V": w.V, "input_dtype": w.dtype,
             "ignored_rows": w.n_ignored, "targets": w.t_dist,
@@ -277,9 +339,10 @@ def main():
     ap.add_argument("--impl", default="flce", choices=["flce", "reference"])
     ap.add_argument("--ce-dtype", default="bf16", choices=["bf16", "fp32"],
                     help="element type of the logits for --op ce_logits")
-    ap.add_argument("--op", default="flce", choices=["flce", "ce_logits"],
-                    help="flce: the fused path (default); ce_logits: cross-entropy on "
-                         "logits already in HBM (logits = X W^T of the workload, bf16)")
+    ap.add_argument("--op", default="flce", choices=["flce", "fwd", "ce_logits"],
+                    help="flce: the fused path (default); fwd: the loss-only path "
+                         "(flce_fwd); ce_logits: cross-entropy on logits already in HBM "
+                         "(logits = X W^T of the workload)")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--shape", default=None,
                     help="N,H,V: a synthetic case of that size with the workload's recipe "
@@ -303,6 +366,8 @@ def main():
         return run_reference(args, workload)
     if args.op == "ce_logits":
         return run_ce_logits(args, workload)
+    if args.op == "fwd":
+        return run_fwd(args, workload)
 
     import torch
     import torch.distributed as dist
