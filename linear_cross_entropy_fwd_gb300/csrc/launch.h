@@ -102,7 +102,6 @@ cudaError_t launch_transpose_f32(const float* in, int64_t R, int64_t C, int64_t 
                                  cudaStream_t s);
 
 // Cross-entropy on materialised logits.
-constexpr int CE_THREADS = 512;
 struct CeRowsParams {
   const void* logits;     // [N, V] bf16 or fp32
   void* dlogits;          // [N, V] same type, may equal logits; NULL = loss only

@@ -330,20 +330,24 @@ struct CeVec<4> {  // 4 fp32 per 16-byte access
 // Without the hints the L2 hit rate of the second read was 6.9% (bf16
 // 8192 x 128256): the kernel moved about 1.5x the algorithmic bytes.
 //
-// Rows in flight (CTAs per SM) and 16-byte loads in flight per thread, by
-// element size, measured on 8192 x 128256 logits (TB/s of algorithmic
-// bytes): bf16 2 CTAs x 6 loads 4.81, 2 x 4 4.77, 3 x 4 4.50, 2 x 8 4.12,
-// 1 x 8 3.47; fp32 1 x 8 4.89, 2 x 4 4.73, 2 x 8 4.69, 1 x 16 4.65,
-// 3 x 4 4.52.
+// Threads per CTA, rows in flight (CTAs per SM) and 16-byte loads in flight
+// per thread, by element size, measured on 8192 x 128256 logits (TB/s of
+// algorithmic bytes):
+//   bf16  512 x 2 x 6 4.81, 512 x 2 x 4 4.77, 256 x 4 x 6 4.46,
+//         512 x 3 x 4 4.50, 1024 x 1 x 4 4.03, 512 x 1 x 8 3.47;
+//   fp32  1024 x 1 x 8 5.35, 1024 x 1 x 4 5.17, 512 x 1 x 8 4.89,
+//         512 x 2 x 4 4.73, 256 x 2 x 8 4.61.
 template <int ELT>
 struct CeRowShape;
 template <>
 struct CeRowShape<2> {
+  static constexpr int kThreads = 512;
   static constexpr int kCtasPerSm = 2;
   static constexpr int kDepth = 6;
 };
 template <>
 struct CeRowShape<4> {
+  static constexpr int kThreads = 1024;
   static constexpr int kCtasPerSm = 1;
   static constexpr int kDepth = 8;
 };
@@ -354,12 +358,13 @@ struct CeRowShape<4> {
 // dS is wanted): the row again (from L2: it was just read), and
 // dS = valid (2^(S log2 e - lse2) - [j = t]) * grad_scale / n.
 template <int ELT>
-__global__ void __launch_bounds__(CE_THREADS, CeRowShape<ELT>::kCtasPerSm)
+__global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kCtasPerSm)
     ce_rows_kernel(const CeRowsParams p) {
   constexpr int kCeDepth = CeRowShape<ELT>::kDepth;
+  constexpr int kThreads = CeRowShape<ELT>::kThreads;
   using Vec = CeVec<ELT>;
   constexpr float kLog2e = 1.4426950408889634f;
-  __shared__ float s_m[CE_THREADS / 32], s_l[CE_THREADS / 32];
+  __shared__ float s_m[kThreads / 32], s_l[kThreads / 32];
   __shared__ float s_lse2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool vec = p.vectorized;
@@ -376,11 +381,11 @@ __global__ void __launch_bounds__(CE_THREADS, CeRowShape<ELT>::kCtasPerSm)
       // kCeDepth independent 16-byte loads in flight per thread
       const uint4* rv = reinterpret_cast<const uint4*>(row);
       int64_t k = threadIdx.x;
-      for (; k + (kCeDepth - 1) * CE_THREADS < nvec; k += kCeDepth * CE_THREADS) {
+      for (; k + (kCeDepth - 1) * kThreads < nvec; k += kCeDepth * kThreads) {
         uint4 u[kCeDepth];
 #pragma unroll
         for (int q = 0; q < kCeDepth; ++q)
-          u[q] = ld_nc_hint(rv + k + q * CE_THREADS, pol_keep);
+          u[q] = ld_nc_hint(rv + k + q * kThreads, pol_keep);
         // the batch's max first: one rescale per batch, then one exp2 and one
         // add per element
         float f[kCeDepth][Vec::kPer];
@@ -401,14 +406,14 @@ __global__ void __launch_bounds__(CE_THREADS, CeRowShape<ELT>::kCtasPerSm)
 #pragma unroll
           for (int e = 0; e < Vec::kPer; ++e) l += fast_exp2(fmaf(f[q][e], kLog2e, -m));
       }
-      for (; k < nvec; k += CE_THREADS) {
+      for (; k < nvec; k += kThreads) {
         float f[Vec::kPer];
         Vec::unpack(ld_nc_hint(rv + k, pol_keep), f);
 #pragma unroll
         for (int e = 0; e < Vec::kPer; ++e) online_add(m, l, f[e] * kLog2e);
       }
     } else {
-      for (int64_t j = threadIdx.x; j < p.V; j += CE_THREADS)
+      for (int64_t j = threadIdx.x; j < p.V; j += kThreads)
         online_add(m, l, Vec::load1(row, j) * kLog2e);
     }
 #pragma unroll
@@ -424,7 +429,7 @@ __global__ void __launch_bounds__(CE_THREADS, CeRowShape<ELT>::kCtasPerSm)
     __syncthreads();
     if (threadIdx.x == 0) {
       float M = s_m[0], L = s_l[0];
-      for (int w = 1; w < CE_THREADS / 32; ++w) online_merge(M, L, s_m[w], s_l[w]);
+      for (int w = 1; w < kThreads / 32; ++w) online_merge(M, L, s_m[w], s_l[w]);
       const float lse2 = M + fast_log2(L);
       s_lse2 = lse2;
       p.partial[r] = lse2;
@@ -442,16 +447,16 @@ __global__ void __launch_bounds__(CE_THREADS, CeRowShape<ELT>::kCtasPerSm)
         const uint4* rv = reinterpret_cast<const uint4*>(row);
         uint4* ov = reinterpret_cast<uint4*>(out);
         int64_t k = threadIdx.x;
-        for (; k + (kCeDepth - 1) * CE_THREADS < nvec; k += kCeDepth * CE_THREADS) {
+        for (; k + (kCeDepth - 1) * kThreads < nvec; k += kCeDepth * kThreads) {
           uint4 u[kCeDepth];
 #pragma unroll
           for (int q = 0; q < kCeDepth; ++q)
-            u[q] = ld_hint(rv + k + q * CE_THREADS, pol_stream);
+            u[q] = ld_hint(rv + k + q * kThreads, pol_stream);
 #pragma unroll
           for (int q = 0; q < kCeDepth; ++q) {
             float f[Vec::kPer];
             Vec::unpack(u[q], f);
-            const int64_t kk = k + q * CE_THREADS;
+            const int64_t kk = k + q * kThreads;
             // the target's position inside this vector, or -1
             const int64_t d = t - kk * Vec::kPer;
             const int tl = (d >= 0 && d < Vec::kPer) ? static_cast<int>(d) : -1;
@@ -462,7 +467,7 @@ __global__ void __launch_bounds__(CE_THREADS, CeRowShape<ELT>::kCtasPerSm)
             st_hint(ov + kk, Vec::pack(f), pol_stream);
           }
         }
-        for (; k < nvec; k += CE_THREADS) {
+        for (; k < nvec; k += kThreads) {
           float f[Vec::kPer];
           Vec::unpack(ld_hint(rv + k, pol_stream), f);
 #pragma unroll
@@ -474,7 +479,7 @@ __global__ void __launch_bounds__(CE_THREADS, CeRowShape<ELT>::kCtasPerSm)
           st_hint(ov + k, Vec::pack(f), pol_stream);
         }
       } else {
-        for (int64_t j = threadIdx.x; j < p.V; j += CE_THREADS) {
+        for (int64_t j = threadIdx.x; j < p.V; j += kThreads) {
           const float x = Vec::load1(row, j);
           const float g =
               valid ? (fast_exp2(fmaf(x, kLog2e, -lse2)) - (j == t ? 1.f : 0.f)) * sc : 0.f;
@@ -493,9 +498,9 @@ cudaError_t launch_ce_rows(const CeRowsParams& p, int elt, int sms, cudaStream_t
   const int64_t cap = static_cast<int64_t>(sms) * (elt == 2 ? Bf16::kCtasPerSm : F32::kCtasPerSm);
   const int64_t blocks = p.N < cap ? p.N : cap;
   if (elt == 2)
-    ce_rows_kernel<2><<<static_cast<unsigned>(blocks), CE_THREADS, 0, s>>>(p);
+    ce_rows_kernel<2><<<static_cast<unsigned>(blocks), Bf16::kThreads, 0, s>>>(p);
   else
-    ce_rows_kernel<4><<<static_cast<unsigned>(blocks), CE_THREADS, 0, s>>>(p);
+    ce_rows_kernel<4><<<static_cast<unsigned>(blocks), F32::kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
