@@ -333,8 +333,9 @@ struct CeVec<4> {  // 4 fp32 per 16-byte access
 // Threads per CTA, rows in flight (CTAs per SM) and 16-byte loads in flight
 // per thread, by element size, measured on 8192 x 128256 logits (TB/s of
 // algorithmic bytes):
-//   bf16  512 x 2 x 6 4.81, 512 x 2 x 4 4.77, 256 x 4 x 6 4.46,
-//         512 x 3 x 4 4.50, 1024 x 1 x 4 4.03, 512 x 1 x 8 3.47;
+//   bf16  512 x 2 x 5 4.89, 512 x 2 x 6 4.77-4.81, 512 x 2 x 4 4.77,
+//         384 x 3 x 6 4.50, 512 x 3 x 4 4.50, 256 x 4 x 6 4.46,
+//         768 x 2 x 4 4.30, 1024 x 1 x 4 4.03, 768 x 1 x 6 3.80;
 //   fp32  1024 x 1 x 8 5.35, 1024 x 1 x 4 5.17, 512 x 1 x 8 4.89,
 //         512 x 2 x 4 4.73, 256 x 2 x 8 4.61.
 template <int ELT>
@@ -343,7 +344,7 @@ template <>
 struct CeRowShape<2> {
   static constexpr int kThreads = 512;
   static constexpr int kCtasPerSm = 2;
-  static constexpr int kDepth = 6;
+  static constexpr int kDepth = 5;
 };
 template <>
 struct CeRowShape<4> {
