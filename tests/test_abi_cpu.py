@@ -3,6 +3,8 @@ without a GPU, exports every symbol include/flce.h declares, agrees with the
 binding on the options layout, and plans workspaces as documented."""
 import os
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -85,3 +87,20 @@ def test_product_path_has_no_oracle_import():
                 src = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in src.replace("oracle/", ""), f
                 assert "flce_synth" not in src, f
+
+
+@pytest.mark.parametrize("std,lang", [("c99", "c"), ("c++11", "c++")])
+def test_header_is_plain_c(tmp_path, std, lang):
+    """include/flce.h needs no CUDA or C++ header: a C99 program (and a C++11
+    one) that fills the options and names every entry point compiles."""
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    calls = "\n".join(f"  (void)&{n};" for n in _declared())
+    src = tmp_path / ("h.c" if lang == "c" else "h.cpp")
+    src.write_text('#include "flce.h"\nint main(void) {\n  flce_opts o;\n'
+                   '  flce_opts_init(&o);\n' + calls + "\n  return 0;\n}\n")
+    r = subprocess.run([cc, f"-std={std}", "-Wall", "-Wextra", "-Werror", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
