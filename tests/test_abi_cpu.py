@@ -78,6 +78,22 @@ def test_workspace_plans(lib):
     assert flce.flce_workspace_bytes(10, 8, 5, vocab_chunk=300) == 0
 
 
+@pytest.mark.parametrize("name,vc", [
+    ("small_head_2048x2048x32000", 12032),        # 64 MiB budget floor: 3 chunks
+    ("llama3_8b_head_8192x4096x128256", 4864),    # pass 2 / dW fill 8 / 4 whole waves
+    ("qwen2_7b_head_16384x3584x152064", 9728),
+    ("long_context_65536x4096x128256", 4864),
+])
+def test_default_chunk_widths(lib, name, vc):
+    """The planner's default chunk width for each workload, read back from the
+    workspace size (the G chunk is N x Vc bf16 on top of a fixed part)."""
+    w = WORKLOADS[name]
+    base = flce.flce_workspace_bytes(w.N, w.H, w.V, vocab_chunk=256)
+    ws = flce.flce_workspace_bytes(w.N, w.H, w.V)
+    assert (ws - base) % (w.N * 2) == 0
+    assert 256 + (ws - base) // (w.N * 2) == vc
+
+
 def test_product_path_has_no_oracle_import():
     """The CUDA package never reaches into the oracle or the generator."""
     pkg = os.path.join(ROOT, "linear_cross_entropy_fwd_gb300")
