@@ -132,3 +132,49 @@ def test_llama3_linearity_and_determinism(cuda_lib, workload_cache):
     # dX rows of each half, rescaled to the full normaliser
     assert_grad(full[2][:h].float().cpu().numpy(),
                 (a[2].float() * na / nf).cpu().numpy(), "dX first half")
+
+
+def test_llama3_loss_only_matches_full_call(cuda_lib, workload_cache):
+    """flce_fwd runs the same pass 1 and combine as the full call: the loss,
+    the count and the per-row lse agree bit for bit at full size."""
+    name = "llama3_8b_head_8192x4096x128256"
+    w = WORKLOADS[name]
+    X, W, t = _inputs(workload_cache, name)
+    Xd, Wd, td = X.to(DEV), W.to(DEV), t.to(DEV)
+    lse_a = torch.empty(w.N, device=DEV)
+    lse_b = torch.empty(w.N, device=DEV)
+    full = cuda_lib.flce_fwd_bwd_ex(Xd, Wd, td, IGN, sync=True, lse_out=lse_a)
+    loss, nval = cuda_lib.flce_fwd(Xd, Wd, td, IGN, sync=True, lse_out=lse_b)
+    assert loss.item() == full[0].item() and int(nval.item()) == int(full[1].item())
+    assert torch.equal(lse_a, lse_b)
+
+
+def test_llama3_ce_on_materialised_logits_sampled_rows(cuda_lib, workload_cache):
+    """Cross-entropy on the full 8192 x 128256 bf16 logits of the workload
+    (S = X W^T by cuBLAS, input staging only): sampled rows of lse, row loss
+    and dS against the oracle on those rows, the count against the closed
+    form, and sum_j dS_ij = 0 on every row."""
+    name = "llama3_8b_head_8192x4096x128256"
+    w = WORKLOADS[name]
+    X, W, t = _inputs(workload_cache, name)
+    S = (X.to(DEV) @ W.to(DEV).t()).contiguous()
+    td = t.to(DEV)
+    lse = torch.empty(w.N, device=DEV)
+    rows_out = torch.empty(w.N, device=DEV)
+    loss, nval, dS = cuda_lib.flce_ce_fwd_bwd(S, td, IGN, sync=True, lse_out=lse,
+                                              loss_rows_out=rows_out)
+    n = int(nval.item())
+    assert n == GOLDEN["ignored_counts"][name]
+    rows = _sample_rows(t, seed=w.seed)
+    Sr = S[rows].cpu()
+    ref = oracle.ce(Sr, t[rows], IGN)
+    n_sub = ref["n_valid"]
+    assert_loss(lse[rows].cpu().numpy(), ref["lse"], "lse rows")
+    assert_loss(rows_out[rows].cpu().numpy(), ref["loss_rows"], "row losses")
+    # the oracle normalises the subset by its own count
+    assert_grad(dS[rows].float().cpu().numpy() * n / n_sub, ref["dS"], "dS rows")
+    rl = rows_out.double()
+    assert abs(loss.item() - rl.sum().item() / n) <= 1e-5 * loss.item()
+    row_sums = dS.float().sum(dim=1).abs()
+    # bf16 rounding of the target entry alone can leave 2^-9 / n per row
+    assert (row_sums <= 1e-2 / n).all(), "a dS row does not sum to ~0"
