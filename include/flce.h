@@ -109,7 +109,7 @@ typedef struct flce_opts {
   size_t workspace_bytes;   /* size of `workspace` */
   size_t workspace_budget;  /* planner budget when workspace == NULL; 0 = one
                                sixteenth of the N x V fp32 logits, but at
-                               least 64 MiB */
+                               least 96 MiB */
   int64_t vocab_chunk;      /* vocabulary columns per chunk; 0 = planner;
                                otherwise a positive multiple of 256 */
   float grad_scale;         /* multiplies G, hence dX and dW (default 1) */

@@ -212,7 +212,7 @@ constexpr int64_t kMinChunk = 2048;
 // The default budget never goes below this: where one sixteenth of the
 // logits is smaller, the fixed part alone (the fp32 dX accumulator) can
 // exceed it and the chunk loop would be all launch overhead.
-constexpr size_t kBudgetFloor = size_t{64} << 20;
+constexpr size_t kBudgetFloor = size_t{96} << 20;
 // Scheduling units the planner assumes (GB300: 152 SMs = 76 CTA pairs), so
 // that a plan, and flce_workspace_bytes(), do not depend on which device
 // (if any) is current when it is made.

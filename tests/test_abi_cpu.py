@@ -79,7 +79,7 @@ def test_workspace_plans(lib):
 
 
 @pytest.mark.parametrize("name,vc", [
-    ("small_head_2048x2048x32000", 12032),        # 64 MiB budget floor: 3 chunks
+    ("small_head_2048x2048x32000", 20224),        # 96 MiB budget floor: 2 chunks
     ("llama3_8b_head_8192x4096x128256", 4864),    # pass 2 / dW fill 8 / 4 whole waves
     ("qwen2_7b_head_16384x3584x152064", 9728),
     ("long_context_65536x4096x128256", 4864),
