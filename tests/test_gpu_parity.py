@@ -136,6 +136,27 @@ def test_launch_sequence(cuda_lib):
     assert kinds == ["logits_lse", "combine"] + ["logits_grad", "dw", "dx"] * 3 + ["convert"]
 
 
+def test_concurrent_calls_on_two_streams(cuda_lib):
+    """Calls are reentrant: two asynchronous calls in flight at once on two
+    streams, each with the library's own scratch, give exactly the result of
+    a lone call (the combine's ticket and scalars live in each call's
+    scratch)."""
+    X, W, t = make_case(700, 256, 6000, "bf16", seed=19, ignore_num=25)
+    Xd, Wd, td = _gpu(X, W, t)
+    ref = cuda_lib.flce_fwd_bwd_ex(Xd, Wd, td, IGN, sync=True, vocab_chunk=1024)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    torch.cuda.synchronize()
+    for k, st in enumerate(streams):
+        with torch.cuda.stream(st):
+            for _ in range(3):  # several calls queued on each stream
+                outs.append(cuda_lib.flce_fwd_bwd_ex(Xd, Wd, td, IGN, vocab_chunk=1024))
+    torch.cuda.synchronize()
+    for loss, nval, dX, dW in outs:
+        assert loss.item() == ref[0].item() and int(nval.item()) == int(ref[1].item())
+        assert torch.equal(dX, ref[2]) and torch.equal(dW, ref[3])
+
+
 def test_all_ignored_gives_zero(cuda_lib):
     X, W, _ = make_case(64, 64, 512, "bf16", seed=12)
     t = torch.full((64,), IGN, dtype=torch.int64)
