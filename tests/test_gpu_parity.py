@@ -157,6 +157,23 @@ def test_concurrent_calls_on_two_streams(cuda_lib):
         assert torch.equal(dX, ref[2]) and torch.equal(dW, ref[3])
 
 
+def test_workspace_budget_is_honoured(cuda_lib):
+    """A caller budget below what one 2048-column chunk needs gets the
+    2048-column plan; the result matches the oracle."""
+    X, W, t = make_case(300, 128, 5000, "bf16", seed=20, ignore_num=10)
+    info = {}
+    ref = oracle.flce(X, W, t, IGN)
+    loss, nval, dX, dW = cuda_lib.flce_fwd_bwd_ex(*_gpu(X, W, t), IGN, sync=True,
+                                                  workspace_budget=1 << 20, info=info)
+    assert info["vocab_chunk"] == 2048
+    assert info["workspace_bytes"] == cuda_lib.flce_workspace_bytes(300, 128, 5000, True,
+                                                                    vocab_chunk=2048)
+    assert int(nval.item()) == ref["n_valid"]
+    assert_loss(loss.item(), ref["loss"])
+    assert_grad(dX.float().cpu().numpy(), ref["dX"], "dX")
+    assert_grad(dW.cpu().numpy(), ref["dW"], "dW")
+
+
 def test_all_ignored_gives_zero(cuda_lib):
     X, W, _ = make_case(64, 64, 512, "bf16", seed=12)
     t = torch.full((64,), IGN, dtype=torch.int64)
