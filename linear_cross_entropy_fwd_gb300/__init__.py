@@ -164,6 +164,23 @@ def _check_inputs(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor, device
             raise ValueError(f"{name} must be a CUDA tensor")
 
 
+def _check_out(t: torch.Tensor, shape, dtype: torch.dtype, device, name: str) -> None:
+    """An output buffer the library writes: exact shape, dtype, device, and
+    contiguous (the library is given only its address)."""
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != device:
+        raise ValueError(f"{name} must be a {dtype} tensor of shape {tuple(shape)} on {device}, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _check_row_outs(N: int, device, lse_out, loss_rows_out) -> None:
+    if lse_out is not None:
+        _check_out(lse_out, (N,), torch.float32, device, "lse_out")
+    if loss_rows_out is not None:
+        _check_out(loss_rows_out, (N,), torch.float32, device, "loss_rows_out")
+
+
 def flce_fwd_bwd_ex(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor,
                     ignore_index: int = -100, *, dX: torch.Tensor | None = None,
                     dW: torch.Tensor | None = None, sync: bool = False,
@@ -187,6 +204,11 @@ def flce_fwd_bwd_ex(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor,
         dX = torch.empty_like(X)
     if dW is None:
         dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+    _check_out(dX, (N, H), X.dtype, dev, "dX")
+    _check_out(dW, (V, H), torch.float32, dev, "dW")
+    _check_row_outs(N, dev, lse_out, loss_rows_out)
+    if workspace is not None:
+        _check_out(workspace, (workspace.numel(),), workspace.dtype, dev, "workspace")
     loss = torch.empty((), dtype=torch.float32, device=dev)
     nval = torch.empty((), dtype=torch.int64, device=dev)
     status = torch.zeros((), dtype=torch.int32, device=dev)
@@ -210,9 +232,10 @@ def flce_fwd_bwd_ex(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor,
     o.workspace_used = ctypes.pointer(used)
     o.vocab_chunk_used = ctypes.pointer(vcu)
     keep = _attach_trace(o, trace)
-    st = lib.flce_fwd_bwd_ex(X.data_ptr(), W.data_ptr(), target.data_ptr(), N, H, V,
-                             int(ignore_index), None, dX.data_ptr(), dW.data_ptr(),
-                             ctypes.byref(o))
+    with torch.cuda.device(dev):
+        st = lib.flce_fwd_bwd_ex(X.data_ptr(), W.data_ptr(), target.data_ptr(), N, H, V,
+                                 int(ignore_index), None, dX.data_ptr(), dW.data_ptr(),
+                                 ctypes.byref(o))
     del keep
     _check(st)
     if info is not None:
@@ -234,8 +257,10 @@ def flce_fwd_bwd(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor,
     dW = torch.empty((V, H), dtype=torch.float32, device=X.device)
     loss = ctypes.c_float(0.0)
     torch.cuda.current_stream(X.device).synchronize()  # the C call uses the default stream
-    st = lib.flce_fwd_bwd(X.data_ptr(), W.data_ptr(), target.data_ptr(), N, H, V,
-                          int(ignore_index), ctypes.byref(loss), dX.data_ptr(), dW.data_ptr())
+    with torch.cuda.device(X.device):
+        st = lib.flce_fwd_bwd(X.data_ptr(), W.data_ptr(), target.data_ptr(), N, H, V,
+                              int(ignore_index), ctypes.byref(loss), dX.data_ptr(),
+                              dW.data_ptr())
     _check(st)
     return loss.value, dX, dW
 
@@ -250,6 +275,7 @@ def flce_fwd(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor, ignore_inde
     N, H = X.shape
     V = W.shape[0]
     dev = X.device
+    _check_row_outs(N, dev, lse_out, loss_rows_out)
     loss = torch.empty((), dtype=torch.float32, device=dev)
     nval = torch.empty((), dtype=torch.int64, device=dev)
     status = torch.zeros((), dtype=torch.int32, device=dev)
@@ -266,8 +292,9 @@ def flce_fwd(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor, ignore_inde
     used = ctypes.c_size_t(0)
     o.workspace_used = ctypes.pointer(used)
     keep = _attach_trace(o, trace)
-    st = lib.flce_fwd(X.data_ptr(), W.data_ptr(), target.data_ptr(), N, H, V,
-                      int(ignore_index), None, ctypes.byref(o))
+    with torch.cuda.device(dev):
+        st = lib.flce_fwd(X.data_ptr(), W.data_ptr(), target.data_ptr(), N, H, V,
+                          int(ignore_index), None, ctypes.byref(o))
     del keep
     _check(st)
     if info is not None:
@@ -298,11 +325,18 @@ def flce_fwd_noalloc(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor,
         n_valid = torch.empty((), dtype=torch.int64, device=dev)
     if status is None:
         status = torch.empty((), dtype=torch.int32, device=dev)
-    st = lib.flce_fwd_noalloc(X.data_ptr(), W.data_ptr(), target.data_ptr(), N, H, V,
-                              int(ignore_index), _dtype_code(X), loss.data_ptr(),
-                              None if lse_out is None else lse_out.data_ptr(),
-                              n_valid.data_ptr(), status.data_ptr(),
-                              torch.cuda.current_stream(dev).cuda_stream)
+    _check_out(loss, (), torch.float32, dev, "loss")
+    _check_out(n_valid, (), torch.int64, dev, "n_valid")
+    _check_out(status, (), torch.int32, dev, "status")
+    if lse_out is not None:
+        _check_out(lse_out, (N,), torch.float32, dev, "lse_out")
+    # the library picks its static scratch by the current device
+    with torch.cuda.device(dev):
+        st = lib.flce_fwd_noalloc(X.data_ptr(), W.data_ptr(), target.data_ptr(), N, H, V,
+                                  int(ignore_index), _dtype_code(X), loss.data_ptr(),
+                                  None if lse_out is None else lse_out.data_ptr(),
+                                  n_valid.data_ptr(), status.data_ptr(),
+                                  torch.cuda.current_stream(dev).cuda_stream)
     _check(st)
     return loss, n_valid, status
 
@@ -335,6 +369,9 @@ def flce_ce_fwd_bwd(logits: torch.Tensor, target: torch.Tensor, ignore_index: in
             dlogits = torch.empty_like(logits)
     else:
         dlogits = None
+    if dlogits is not None:
+        _check_out(dlogits, (N, V), logits.dtype, dev, "dlogits")
+    _check_row_outs(N, dev, lse_out, loss_rows_out)
     loss = torch.empty((), dtype=torch.float32, device=dev)
     nval = torch.empty((), dtype=torch.int64, device=dev)
     status = torch.zeros((), dtype=torch.int32, device=dev)
@@ -352,9 +389,11 @@ def flce_ce_fwd_bwd(logits: torch.Tensor, target: torch.Tensor, ignore_index: in
     used = ctypes.c_size_t(0)
     o.workspace_used = ctypes.pointer(used)
     keep = _attach_trace(o, trace)
-    st = lib.flce_ce_fwd_bwd(logits.data_ptr(), target.data_ptr(), N, V, int(ignore_index),
-                             None, None if dlogits is None else dlogits.data_ptr(),
-                             ctypes.byref(o))
+    with torch.cuda.device(dev):
+        st = lib.flce_ce_fwd_bwd(logits.data_ptr(), target.data_ptr(), N, V,
+                                 int(ignore_index), None,
+                                 None if dlogits is None else dlogits.data_ptr(),
+                                 ctypes.byref(o))
     del keep
     _check(st)
     if info is not None:

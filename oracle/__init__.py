@@ -54,7 +54,7 @@ def _load():
         if _lib is None:
             lib = ctypes.CDLL(build())
             p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-            lib.oracle_flce.argtypes = [p, p, i32, p, i64, i64, i64, i64,
+            lib.oracle_flce.argtypes = [p, p, i32, p, i64, i64, i64, i64, i64,
                                         p, p, p, p, p, p]
             lib.oracle_flce.restype = i32
             lib.oracle_flce_rows.argtypes = [p, p, i32, p, i64, i64, i64, i64,
@@ -127,8 +127,13 @@ def _check(rc):
         raise OracleError("target outside [0, V) that is not the ignore index")
 
 
-def flce(X, W, t, ignore_index: int = -100, grads: bool = True) -> dict:
-    """Full problem: loss, n_valid, lse [N], loss_rows [N], dX [N,H], dW [V,H]."""
+def flce(X, W, t, ignore_index: int = -100, grads: bool = True,
+         norm_count: int = 0) -> dict:
+    """Full problem: loss, n_valid, lse [N], loss_rows [N], dX [N,H], dW [V,H].
+
+    ``norm_count > 0`` makes this call one data-parallel shard of a larger
+    batch: the mean and G are divided by that count (the whole batch's valid
+    rows) instead of by this call's own ``n_valid``."""
     x, tx = _as_matrix(X)
     w, tw = _as_matrix(W)
     if tx != tw:
@@ -144,7 +149,7 @@ def flce(X, W, t, ignore_index: int = -100, grads: bool = True) -> dict:
     dX = np.zeros((N, H)) if grads else None
     dW = np.zeros((V, H)) if grads else None
     rc = _load().oracle_flce(_ptr(x), _ptr(w), tx, _ptr(tt), N, H, V, int(ignore_index),
-                             _ptr(loss), _ptr(nv), _ptr(lse), _ptr(lrows),
+                             int(norm_count), _ptr(loss), _ptr(nv), _ptr(lse), _ptr(lrows),
                              _ptr(dX), _ptr(dW))
     _check(rc)
     return {"loss": float(loss[0]), "n_valid": int(nv[0]), "lse": lse,

@@ -20,7 +20,12 @@
  *
  * Readings taken where the pages are silent: mean over valid rows; when
  * n_valid == 0 the loss and both gradients are 0; a target outside [0, V)
- * that is not the ignore index is an error (return code 2).
+ * that is not the ignore index is an error (return code 2).  A call that is
+ * one data-parallel shard of a larger batch (the overview's FSDP / DeepSpeed
+ * compatibility, "Alta Compatibilidade") may give the whole batch's valid
+ * count as norm_count > 0: the mean and G are then divided by it instead of
+ * by this call's own count, so the shards' losses, dW and dX rows add up to
+ * the whole batch's.
  *
  * Arithmetic: every product and sum in double, in the order written below
  * (sums over H and V run from index 0 upward).  The max-shift inside lse is
@@ -116,18 +121,21 @@ int oracle_num_threads(void) {
 /*
  * Full problem.  Outputs: *loss, *n_valid, lse[N] (may be NULL),
  * loss_rows[N] per-row lse_i - S_{i,t_i} (0 for ignored rows; may be NULL),
- * dX[N*H] and dW[V*H] (either may be NULL to skip it).
+ * dX[N*H] and dW[V*H] (either may be NULL to skip it).  norm_count <= 0
+ * divides by this call's valid count n_valid; norm_count > 0 divides by it
+ * instead (a shard of a larger batch).
  */
 int oracle_flce(const void *X, const void *W, int type, const int64_t *t,
                 int64_t N, int64_t H, int64_t V, int64_t ignore_index,
-                double *loss, int64_t *n_valid, double *lse, double *loss_rows,
-                double *dX, double *dW) {
+                int64_t norm_count, double *loss, int64_t *n_valid, double *lse,
+                double *loss_rows, double *dX, double *dW) {
   if (N < 0 || H <= 0 || V <= 0 || !loss || !n_valid) return 1;
   if (N > 0 && (!X || !W || !t)) return 1;
   int rc = check_targets(t, N, V, ignore_index);
   if (rc) return rc;
   const int64_t nv = oracle_count_valid(t, N, ignore_index);
   *n_valid = nv;
+  const double den = norm_count > 0 ? (double)norm_count : (double)nv;
 
   double *lse_all = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
   double *lrow = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
@@ -149,7 +157,7 @@ int oracle_flce(const void *X, const void *W, int type, const int64_t *t,
   /* loss: ordered sum over rows, then the mean over valid rows */
   double acc = 0.0;
   for (int64_t i = 0; i < N; ++i) acc += lrow[i];
-  *loss = nv > 0 ? acc / (double)nv : 0.0;
+  *loss = nv > 0 ? acc / den : 0.0;
   if (lse) memcpy(lse, lse_all, (size_t)N * sizeof(double));
   if (loss_rows) memcpy(loss_rows, lrow, (size_t)N * sizeof(double));
 
@@ -164,7 +172,7 @@ int oracle_flce(const void *X, const void *W, int type, const int64_t *t,
         if (t[i] == ignore_index) continue;
         double g = exp(logit(X, W, type, H, i, j) - lse_all[i]) -
                    (t[i] == j ? 1.0 : 0.0);
-        g /= (double)nv;
+        g /= den;
         for (int64_t h = 0; h < H; ++h) dwj[h] += g * elem(X, type, i * H + h);
       }
     }
@@ -183,7 +191,7 @@ int oracle_flce(const void *X, const void *W, int type, const int64_t *t,
         logit_row(X, W, type, H, V, i, srow);
         for (int64_t j = 0; j < V; ++j) {
           double g = exp(srow[j] - lse_all[i]) - (t[i] == j ? 1.0 : 0.0);
-          g /= (double)nv;
+          g /= den;
           for (int64_t h = 0; h < H; ++h) dxi[h] += g * elem(W, type, j * H + h);
         }
       }

@@ -40,3 +40,30 @@ def assert_grad(got, ref, what):
         return
     assert err <= GRAD_MAX_REL * mx, f"{what}: max|d| {err:.3e} > {GRAD_MAX_REL} * {mx:.3e}"
     assert cos >= GRAD_COS, f"{what}: cosine {cos:.6f} < {GRAD_COS}"
+
+
+def assert_grad_blocks(got, ref, what, rows_per_block: int = 4096):
+    """assert_grad for a large gradient, block of rows by block of rows (no
+    full float64 copy of ``got``): the same criteria (max|d| against max|ref|
+    over the whole array, and the cosine over the whole array).  ``got`` is a
+    torch tensor (any device) or a numpy array, ``ref`` a float64 array of the
+    same shape."""
+    import torch
+    R = ref.shape[0]
+    err = mx = dot = ng2 = nr2 = 0.0
+    for a in range(0, R, rows_per_block):
+        b = min(a + rows_per_block, R)
+        g = got[a:b]
+        g = g.double().cpu().numpy() if isinstance(g, torch.Tensor) else np.asarray(g, np.float64)
+        r = ref[a:b]
+        err = max(err, float(np.abs(g - r).max()) if g.size else 0.0)
+        mx = max(mx, float(np.abs(r).max()) if r.size else 0.0)
+        dot += float((g * r).sum())
+        ng2 += float((g * g).sum())
+        nr2 += float((r * r).sum())
+    if mx == 0.0:
+        assert err == 0.0, f"{what}: reference is zero but max|got| = {err:.3e}"
+        return
+    cos = dot / np.sqrt(ng2 * nr2) if ng2 > 0 and nr2 > 0 else 0.0
+    assert err <= GRAD_MAX_REL * mx, f"{what}: max|d| {err:.3e} > {GRAD_MAX_REL} * {mx:.3e}"
+    assert cos >= GRAD_COS, f"{what}: cosine {cos:.6f} < {GRAD_COS}"

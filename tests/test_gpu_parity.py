@@ -126,6 +126,57 @@ def test_vocabulary_and_width_extremes(cuda_lib, N, H, V, vc):
     _check_full(cuda_lib, X, W, t, vocab_chunk=vc)
 
 
+def test_more_tiles_than_units_in_every_gemm(cuda_lib):
+    """4096 x 2048 x 8192: 128 dX pair tiles (16 x 8) for 76 CTA pairs, so
+    units run two dX tiles each and the dX GEMM uses both TMEM accumulator
+    buffers and the ring's phase flips across tiles; pass 2 and dW also have
+    more tiles than units.  Once with the planner's chunk width and once with
+    2048-column chunks (dX then takes the fp32 TMA reduce-add path over
+    several tiles per unit).  Every output element against the oracle."""
+    N, H, V = 4096, 2048, 8192
+    X, W, t = make_case(N, H, V, "bf16", seed=4242, ignore_num=3, t_dist="zipf")
+    ref = oracle.flce(X, W, t, IGN)
+    Xd, Wd, td = _gpu(X, W, t)
+    for vc in (0, 2048):
+        info = {}
+        lse = torch.empty(N, device=DEV)
+        loss, nval, dX, dW = cuda_lib.flce_fwd_bwd_ex(Xd, Wd, td, IGN, sync=True,
+                                                      lse_out=lse, vocab_chunk=vc, info=info)
+        assert int(nval.item()) == ref["n_valid"]
+        assert_loss(loss.item(), ref["loss"])
+        assert_loss(lse.cpu().numpy(), ref["lse"], "lse")
+        assert_grad(dX.float().cpu().numpy(), ref["dX"], f"dX (chunk {info['vocab_chunk']})")
+        assert_grad(dW.cpu().numpy(), ref["dW"], f"dW (chunk {info['vocab_chunk']})")
+        if vc:
+            assert info["vocab_chunk"] == vc
+
+
+def test_shift_invariance_with_large_row_offsets(cuda_lib):
+    """W + 1 b^T adds x_i . b to every logit of row i (here up to about +-45):
+    softmax, loss, dW and dX are unchanged because each row of G sums to 0,
+    and lse_i moves by x_i . b.  W and b sit on grids (k/256, |k| <= 16, and
+    m/16, |m| <= 8) on which W + 1 b^T is exact in bf16.  The shifted problem
+    on the GPU must match the oracle's unshifted one."""
+    N, H, V = 300, 2048, 3000
+    g = torch.Generator().manual_seed(77)
+    X, _, t = make_case(N, H, V, "bf16", seed=77, ignore_num=10)
+    Wk = torch.randint(-16, 17, (V, H), generator=g).double() / 256
+    b = torch.randint(-8, 9, (H,), generator=g).double() / 16
+    W = Wk.to(torch.bfloat16)
+    Ws = (Wk + b[None, :]).to(torch.bfloat16)
+    assert torch.equal(Ws.double(), Wk + b[None, :])  # exact in bf16
+    lse = torch.empty(N, device=DEV)
+    loss, nval, dX, dW = cuda_lib.flce_fwd_bwd_ex(*_gpu(X, Ws, t), IGN, sync=True, lse_out=lse)
+    ref = oracle.flce(X, W, t, IGN)
+    shift = (X.double() @ b).numpy()
+    assert np.abs(shift).max() > 20.0
+    assert int(nval.item()) == ref["n_valid"]
+    assert_loss(loss.item(), ref["loss"])
+    assert_loss(lse.cpu().numpy(), ref["lse"] + shift, "lse")
+    assert_grad(dX.float().cpu().numpy(), ref["dX"], "dX")
+    assert_grad(dW.cpu().numpy(), ref["dW"], "dW")
+
+
 def test_launch_sequence(cuda_lib):
     """Per-launch trace of a three-chunk call: pass 1, combine, then pass 2,
     dW and dX per chunk, then the bf16 conversion of dX."""

@@ -380,12 +380,48 @@ def test_subset_functions_against_torch_autograd():
                                rtol=1e-10, atol=1e-16)
 
 
+# ------------------------------------------------------- data-parallel shards
+def test_shard_normaliser():
+    """norm_count > 0 divides by the whole batch's valid count instead of the
+    call's own: equal to the default when it is the call's own count; each
+    shard matches torch float64 autograd of the sum-reduced cross-entropy
+    divided by norm_count; and three row shards' losses and dW add up to the
+    whole batch's while their dX rows stack to its dX."""
+    X, W, t = make_case(41, 12, 70, "fp32", seed=91, ignore_num=9, w_std=0.5)
+    whole = oracle.flce(X, W, t, IGN)
+    n = whole["n_valid"]
+    own = oracle.flce(X, W, t, IGN, norm_count=n)
+    assert own["loss"] == whole["loss"]
+    np.testing.assert_array_equal(own["dW"], whole["dW"])
+    np.testing.assert_array_equal(own["dX"], whole["dX"])
+    parts = np.array_split(np.arange(41), 3)
+    loss_sum, dW_sum, dX_rows = 0.0, np.zeros_like(whole["dW"]), []
+    for rows in parts:
+        Xs, ts = X[rows].contiguous(), t[rows].contiguous()
+        r = oracle.flce(Xs, W, ts, IGN, norm_count=n)
+        assert r["n_valid"] == int((ts != IGN).sum())
+        Xt = Xs.double().requires_grad_(True)
+        Wt = W.double().requires_grad_(True)
+        ref = torch.nn.functional.cross_entropy(torch.nn.functional.linear(Xt, Wt), ts,
+                                                ignore_index=IGN, reduction="sum") / n
+        ref.backward()
+        assert abs(r["loss"] - ref.item()) <= 1e-13 * abs(ref.item())
+        np.testing.assert_allclose(r["dX"], Xt.grad.numpy(), rtol=1e-10, atol=1e-15)
+        np.testing.assert_allclose(r["dW"], Wt.grad.numpy(), rtol=1e-10, atol=1e-15)
+        loss_sum += r["loss"]
+        dW_sum += r["dW"]
+        dX_rows.append(r["dX"])
+    assert abs(loss_sum - whole["loss"]) <= 1e-13 * whole["loss"]
+    np.testing.assert_allclose(dW_sum, whole["dW"], rtol=1e-11, atol=1e-16)
+    np.testing.assert_allclose(np.vstack(dX_rows), whole["dX"], rtol=1e-12, atol=1e-16)
+
+
 # -------------------------------------------------------------- planted mistakes
 MUTATIONS = [
     # (name, original text in flce_oracle.c, planted replacement)
-    ("one-hot sign in dW", "(t[i] == j ? 1.0 : 0.0);\n        g /= (double)nv;",
-     "(t[i] == j ? -1.0 : 0.0);\n        g /= (double)nv;"),
-    ("normaliser N instead of n_valid", "*loss = nv > 0 ? acc / (double)nv : 0.0;\n  if (lse)",
+    ("one-hot sign in dW", "(t[i] == j ? 1.0 : 0.0);\n        g /= den;",
+     "(t[i] == j ? -1.0 : 0.0);\n        g /= den;"),
+    ("normaliser N instead of n_valid", "*loss = nv > 0 ? acc / den : 0.0;\n  if (lse)",
      "*loss = nv > 0 ? acc / (double)N : 0.0;\n  if (lse)"),
     ("transposed operand in dX", "dxi[h] += g * elem(W, type, j * H + h);\n        }\n      }\n      free",
      "dxi[h] += g * elem(X, type, i * H + h);\n        }\n      }\n      free"),
@@ -409,7 +445,8 @@ def test_pins_catch_a_planted_mistake(tmp_path, name, orig, planted):
                     str(p), "-lm"], check=True)
     lib = ctypes.CDLL(str(so))
     vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-    lib.oracle_flce.argtypes = [vp, vp, i32, vp, i64, i64, i64, i64, vp, vp, vp, vp, vp, vp]
+    lib.oracle_flce.argtypes = [vp, vp, i32, vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp,
+                                vp]
     lib.oracle_flce.restype = i32
 
     def run(X, W, t):
@@ -422,7 +459,7 @@ def test_pins_catch_a_planted_mistake(tmp_path, name, orig, planted):
         lse, lr = np.zeros(N), np.zeros(N)
         dX, dW = np.zeros((N, H)), np.zeros((V, H))
         ptr = lambda a: a.ctypes.data_as(vp)  # noqa: E731
-        lib.oracle_flce(ptr(X), ptr(W), 0, ptr(t), N, H, V, IGN, ptr(loss), ptr(nv), ptr(lse),
+        lib.oracle_flce(ptr(X), ptr(W), 0, ptr(t), N, H, V, IGN, 0, ptr(loss), ptr(nv), ptr(lse),
                         ptr(lr), ptr(dX), ptr(dW))
         return loss[0], dX, dW
 
