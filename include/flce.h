@@ -22,8 +22,9 @@
  * Conventions shared by every entry point
  *   - X, W and dX are row-major and contiguous, element type opts->dtype
  *     (bf16 by default, or fp32 computed with tf32 tensor-core products);
- *     dW is fp32; target is int64 [N].  All of them are device pointers owned
- *     by the caller, except in flce_fwd_bwd_host().
+ *     dW is fp32; target is int64 [N] (int32 [N] when opts->target_is_int32
+ *     is set; the pointer is then read as int32_t*).  All of them are device
+ *     pointers owned by the caller, except in flce_fwd_bwd_host().
  *   - X, W, dX and dW must be 16-byte aligned and H * sizeof(element) must be
  *     a multiple of 16 bytes; otherwise FLCE_ERR_ALIGN.
  *   - dX and dW are overwritten, never accumulated into.
@@ -57,7 +58,7 @@
 extern "C" {
 #endif
 
-#define FLCE_VERSION 1
+#define FLCE_VERSION 2
 
 #if defined(__GNUC__)
 #define FLCE_API __attribute__((visibility("default")))
@@ -113,7 +114,8 @@ typedef struct flce_opts {
   int64_t vocab_chunk;      /* vocabulary columns per chunk; 0 = planner;
                                otherwise a positive multiple of 256 */
   float grad_scale;         /* multiplies G, hence dX and dW (default 1) */
-  int32_t reserved0;
+  int32_t target_is_int32;  /* 1: `target` points to int32 ids [N] instead of
+                               int64 (default 0) */
   int64_t norm_count;       /* > 0: normalise by this count instead of the
                                local n (a data-parallel shard normalising by
                                the global count); the loss is then

@@ -47,7 +47,7 @@ class FlceOpts(ctypes.Structure):
         ("workspace_budget", ctypes.c_size_t),
         ("vocab_chunk", ctypes.c_int64),
         ("grad_scale", ctypes.c_float),
-        ("reserved0", ctypes.c_int32),
+        ("target_is_int32", ctypes.c_int32),
         ("norm_count", ctypes.c_int64),
         ("loss_dev", ctypes.c_void_p),
         ("lse_out", ctypes.c_void_p),
@@ -155,13 +155,17 @@ def _check_inputs(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor, device
                          f"target{tuple(target.shape)}")
     if X.dtype != W.dtype:
         raise TypeError("X and W must share one dtype")
-    if target.dtype != torch.int64:
-        raise TypeError("target must be int64")
+    if target.dtype not in (torch.int64, torch.int32):
+        raise TypeError("target must be int64 or int32")
     for name, t in (("X", X), ("W", W), ("target", target)):
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
         if device_needed and not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _is32(target: torch.Tensor) -> int:
+    return 1 if target.dtype == torch.int32 else 0
 
 
 def _check_out(t: torch.Tensor, shape, dtype: torch.dtype, device, name: str) -> None:
@@ -215,7 +219,7 @@ def flce_fwd_bwd_ex(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor,
     o = make_opts(X.dtype, torch.cuda.current_stream(dev).cuda_stream,
                   sync=1 if sync else 0, grad_scale=float(grad_scale),
                   norm_count=int(norm_count), workspace_budget=int(workspace_budget),
-                  vocab_chunk=int(vocab_chunk))
+                  vocab_chunk=int(vocab_chunk), target_is_int32=_is32(target))
     o.dtype = _dtype_code(X)
     o.loss_dev = loss.data_ptr()
     o.n_valid_dev = nval.data_ptr()
@@ -249,8 +253,9 @@ def flce_fwd_bwd(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor,
     Returns (loss: float, dX, dW)."""
     lib = load_library()
     _check_inputs(X, W, target)
-    if X.dtype != torch.bfloat16:
-        raise TypeError("flce_fwd_bwd takes bf16 inputs; use flce_fwd_bwd_ex for fp32")
+    if X.dtype != torch.bfloat16 or target.dtype != torch.int64:
+        raise TypeError("flce_fwd_bwd takes bf16 inputs and int64 targets; use "
+                        "flce_fwd_bwd_ex for fp32 inputs or int32 targets")
     N, H = X.shape
     V = W.shape[0]
     dX = torch.empty_like(X)
@@ -280,7 +285,7 @@ def flce_fwd(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor, ignore_inde
     nval = torch.empty((), dtype=torch.int64, device=dev)
     status = torch.zeros((), dtype=torch.int32, device=dev)
     o = make_opts(X.dtype, torch.cuda.current_stream(dev).cuda_stream, sync=1 if sync else 0,
-                  norm_count=int(norm_count))
+                  norm_count=int(norm_count), target_is_int32=_is32(target))
     o.dtype = _dtype_code(X)
     o.loss_dev = loss.data_ptr()
     o.n_valid_dev = nval.data_ptr()
@@ -316,6 +321,8 @@ def flce_fwd_noalloc(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor,
     serialised.  Returns (loss, n_valid, status) device tensors."""
     lib = load_library()
     _check_inputs(X, W, target)
+    if target.dtype != torch.int64:
+        raise TypeError("flce_fwd_noalloc takes int64 targets")
     N, H = X.shape
     V = W.shape[0]
     dev = X.device
@@ -358,8 +365,8 @@ def flce_ce_fwd_bwd(logits: torch.Tensor, target: torch.Tensor, ignore_index: in
     if not (logits.is_cuda and target.is_cuda and logits.is_contiguous()
             and target.is_contiguous()):
         raise ValueError("contiguous CUDA tensors expected")
-    if target.dtype != torch.int64:
-        raise TypeError("target must be int64")
+    if target.dtype not in (torch.int64, torch.int32):
+        raise TypeError("target must be int64 or int32")
     N, V = logits.shape
     dev = logits.device
     if grad:
@@ -377,7 +384,7 @@ def flce_ce_fwd_bwd(logits: torch.Tensor, target: torch.Tensor, ignore_index: in
     status = torch.zeros((), dtype=torch.int32, device=dev)
     o = make_opts(logits.dtype, torch.cuda.current_stream(dev).cuda_stream,
                   sync=1 if sync else 0, grad_scale=float(grad_scale),
-                  norm_count=int(norm_count))
+                  norm_count=int(norm_count), target_is_int32=_is32(target))
     o.dtype = _dtype_code(logits)
     o.loss_dev = loss.data_ptr()
     o.n_valid_dev = nval.data_ptr()
@@ -417,7 +424,7 @@ def flce_fwd_bwd_host(X: torch.Tensor, W: torch.Tensor, target: torch.Tensor,
     if dW is None:
         dW = torch.empty((V, H), dtype=torch.float32)
     loss = ctypes.c_float(0.0)
-    o = make_opts(X.dtype, stream, vocab_chunk=int(vocab_chunk))
+    o = make_opts(X.dtype, stream, vocab_chunk=int(vocab_chunk), target_is_int32=_is32(target))
     o.dtype = _dtype_code(X)
     st = lib.flce_fwd_bwd_host(X.data_ptr(), W.data_ptr(), target.data_ptr(), N, H, V,
                                int(ignore_index), ctypes.byref(loss), dX.data_ptr(),

@@ -18,7 +18,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // and, for the one tile that holds the row's target column, st[row] = S_{i,t_i}.
 struct EpiRowLse {
   struct Params {
-    const int64_t* target;
+    Targets target;
     float* partial;   // [num_vocab_tiles][N]
     float* st;        // [N] target logit
     int64_t N;
@@ -113,7 +113,7 @@ __device__ __forceinline__ void staging_release(const CUtensorMap* map, uint8_t*
 template <int ELT>
 struct EpiGradLogits {
   struct Params {
-    const int64_t* target;
+    Targets target;
     const float* lse2;          // [N]
     const Scalars* scalars;     // scale
     int64_t N;

@@ -413,8 +413,18 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
   float* lse2 = reinterpret_cast<float*>(ws + P.off_lse2);
   float* st = reinterpret_cast<float*>(ws + P.off_st);
   float* partial = reinterpret_cast<float*>(ws + P.off_partial);
+  const Targets tg{target, o.target_is_int32 != 0 ? 1 : 0};
   int rc;
   Tracer tr(o, s);
+  // GEMM launch k of this call takes its tiles from counter k % 3 and zeroes
+  // counter (k + 2) % 3 for the launch two later (the memset clears all three
+  // for the first two launches).
+  int n_gemm = 0;
+  auto schedule = [&](GemmGrid& g) {
+    g.tile_ctr = &sc->tile_ctr[n_gemm % 3];
+    g.ctr_reset = &sc->tile_ctr[(n_gemm + 2) % 3];
+    ++n_gemm;
+  };
 
   FLCE_CUDA(cudaMemsetAsync(sc, 0, sizeof(Scalars), s));
   if ((rc = tr.start())) return rc;
@@ -435,7 +445,8 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
       g.num_k_blk = static_cast<int32_t>((H + KE - 1) / KE);
       g.b_mn_off = static_cast<int32_t>(t0 * BN);
       g.status = &sc->status;
-      RowLseParams rp{target, partial, st, N, V, static_cast<int32_t>(t0)};
+      schedule(g);
+      RowLseParams rp{tg, partial, st, N, V, static_cast<int32_t>(t0)};
       const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, units);
       FLCE_CUDA(bf16 ? launch_logits_lse_bf16(mX, mW, g, rp, grid, s)
                      : launch_logits_lse_fp32(mX, mW, g, rp, grid, s));
@@ -446,7 +457,7 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
   cp.partial = partial;
   cp.num_vblk = static_cast<int32_t>(P.num_vblk);
   cp.st = st;
-  cp.target = target;
+  cp.target = tg;
   cp.N = N;
   cp.V = V;
   cp.ignore_index = ignore_index;
@@ -512,7 +523,8 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
           g.num_k_blk = static_cast<int32_t>((H + KE - 1) / KE);
           g.b_mn_off = static_cast<int32_t>(c0);
           g.status = &sc->status;
-          GradLogitsParams gp{target, lse2, sc, N, V, ignore_index, c0};
+          schedule(g);  // operands are inputs; the epilogue waits before writing G
+          GradLogitsParams gp{tg, lse2, sc, N, V, ignore_index, c0};
           const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, units);
           FLCE_CUDA(bf16 ? launch_logits_grad_bf16(mX_K, mW_K, mG_st, g, gp, grid, s)
                          : launch_logits_grad_fp32(mX_K, mW_K, mG_st, g, gp, grid, s));
@@ -532,6 +544,8 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
           g.num_k_blk = static_cast<int32_t>((N + KE - 1) / KE);
           g.status = &sc->status;
           g.raster_n = 1;  // a slab of G_c rows with all of X stays in L2
+          g.wait_operands = 1;  // G_c comes from the launch just before
+          schedule(g);
           StoreParams sp{0, static_cast<int32_t>(c0), 0};
           const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, units);
           FLCE_CUDA(bf16 ? launch_dw_bf16(mA4, mB4, mdW, g, sp, grid, s)
@@ -554,6 +568,9 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
           g.b_k_off = bf16 ? static_cast<int32_t>(c0) : 0;
           g.raster_n = 1;  // a slab of G_c rows with all of W[c] stays in L2
           g.status = &sc->status;
+          // G_c comes from two launches back (the dW launch is in between),
+          // so the operand loads start at once
+          schedule(g);
           StoreParams sp{0, 0, c > 0 ? 1 : 0};
           const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, units);
           FLCE_CUDA(bf16 ? launch_dx_bf16(mA5, mB5, mdX, g, sp, grid, s)
@@ -675,6 +692,7 @@ int ce_entry(const void* logits, const int64_t* target, int64_t N, int64_t V,
     return FLCE_ERR_ARG;
   }
   const int elt = (o.dtype == FLCE_FP32) ? 4 : 2;
+  const Targets tg{target, o.target_is_int32 != 0 ? 1 : 0};
   DeviceInfo D;
   int rc = device_info(o.dtype, &D);
   if (rc) return rc;
@@ -715,7 +733,7 @@ int ce_entry(const void* logits, const int64_t* target, int64_t N, int64_t V,
   if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemsetAsync(scalars)");
   if (rc == FLCE_OK) rc = tr.start();
   if (rc == FLCE_OK && N > 0) {
-    e = launch_ce_count(target, N, V, ignore_index, sc, D.sms, s);
+    e = launch_ce_count(tg, N, V, ignore_index, sc, D.sms, s);
     if (e != cudaSuccess) rc = cuda_fail(e, "ce_count");
     if (rc == FLCE_OK) rc = tr.after(FLCE_TRACE_CE_COUNT);
   }
@@ -723,7 +741,7 @@ int ce_entry(const void* logits, const int64_t* target, int64_t N, int64_t V,
     CeRowsParams cp{};
     cp.logits = logits;
     cp.dlogits = dlogits;
-    cp.target = target;
+    cp.target = tg;
     cp.N = N;
     cp.V = V;
     cp.ignore_index = ignore_index;
@@ -744,7 +762,7 @@ int ce_entry(const void* logits, const int64_t* target, int64_t N, int64_t V,
     cp.partial = reinterpret_cast<float*>(ws + off_part);
     cp.num_vblk = 1;
     cp.st = reinterpret_cast<float*>(ws + off_st);
-    cp.target = target;
+    cp.target = tg;
     cp.N = N;
     cp.V = V;
     cp.ignore_index = ignore_index;
@@ -878,7 +896,8 @@ int flce_fwd_bwd_host(const void* X_host, const void* W_host, const int64_t* tar
   if (rc) return rc;
   const size_t elt = (o.dtype == FLCE_FP32) ? 4 : 2;
   const size_t bx = static_cast<size_t>(N) * H * elt, bw = static_cast<size_t>(V) * H * elt,
-               bt = static_cast<size_t>(N) * 8, bdw = static_cast<size_t>(V) * H * 4;
+               bt = static_cast<size_t>(N) * (o.target_is_int32 ? 4 : 8),
+               bdw = static_cast<size_t>(V) * H * 4;
   cudaStream_t s = static_cast<cudaStream_t>(o.stream);
   const size_t ox = 0, ow = align_up(ox + bx, 256), ot = align_up(ow + bw, 256),
                odx = align_up(ot + bt, 256), odw = align_up(odx + bx, 256),

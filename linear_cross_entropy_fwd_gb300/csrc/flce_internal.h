@@ -24,6 +24,7 @@ constexpr int STAGING_BUF_BYTES = 4096;              // one 32-row x 128-byte TM
 constexpr int STAGING_BYTES = EPI_WARPS * 2 * STAGING_BUF_BYTES;
 constexpr int TMEM_COLS = 2 * BN;                    // two fp32 accumulators of BN columns
 constexpr int SMEM_BARRIER_BYTES = 256;
+constexpr int SCHED_SLOTS = 4;                       // tile indices in flight per CTA
 constexpr int GEMM_SMEM_BYTES =
     1024 + STAGES * (A_STAGE_BYTES + B_STAGE_BYTES) + STAGING_BYTES + SMEM_BARRIER_BYTES;
 
@@ -39,7 +40,11 @@ struct GemmGrid {
   int32_t raster_n;    // 0: M index fastest in the tile order, 1: N index fastest
   int32_t a_l2;        // L2 policy of operand loads: 0 normal, 1 evict first,
   int32_t b_l2;        // 2 evict last
+  int32_t wait_operands;  // 1: an operand is written by the launch just before
+                          // this one, so the loads wait for it to complete
   int32_t* status;     // device status word (FLCE_DEV_* bits)
+  uint32_t* tile_ctr;  // tile counter of this launch (zero at launch)
+  uint32_t* ctr_reset; // counter to zero for the launch two after this one
 };
 
 // Tile t of a launch -> (m block, n block).  The CTAs that run at the same
@@ -56,7 +61,17 @@ __host__ __device__ inline void tile_coords(const GemmGrid& g, int tile, int& m_
   }
 }
 
-// Small device-side scalars of one call.
+// Target ids of a call: int64 (the default) or int32 [N], read as int64.
+struct Targets {
+  const void* p;
+  int32_t is32;
+  __host__ __device__ int64_t operator[](int64_t i) const {
+    return is32 ? static_cast<int64_t>(static_cast<const int32_t*>(p)[i])
+                : static_cast<const int64_t*>(p)[i];
+  }
+};
+
+// Small device-side scalars of one call (cleared before its first kernel).
 struct Scalars {
   int32_t status;
   uint32_t ticket;
@@ -64,6 +79,8 @@ struct Scalars {
   float scale;        // grad_scale / normaliser (0 when nothing is valid)
   float loss;
   double loss_sum;
+  uint32_t tile_ctr[3];  // GEMM launch k takes its tiles from tile_ctr[k % 3]
+  uint32_t pad_;
 };
 
 }  // namespace flce

@@ -8,7 +8,7 @@
 namespace flce {
 
 struct RowLseParams {
-  const int64_t* target;
+  Targets target;
   float* partial;
   float* st;
   int64_t N;
@@ -17,7 +17,7 @@ struct RowLseParams {
 };
 
 struct GradLogitsParams {
-  const int64_t* target;
+  Targets target;
   const float* lse2;
   const Scalars* scalars;
   int64_t N;
@@ -70,7 +70,7 @@ struct CombineParams {
   const float* partial;   // [num_vblk][N]
   int32_t num_vblk;
   const float* st;        // [N]
-  const int64_t* target;  // [N]
+  Targets target;         // [N]
   int64_t N;
   int64_t V;
   int64_t ignore_index;
@@ -105,7 +105,7 @@ cudaError_t launch_transpose_f32(const float* in, int64_t R, int64_t C, int64_t 
 struct CeRowsParams {
   const void* logits;     // [N, V] bf16 or fp32
   void* dlogits;          // [N, V] same type, may equal logits; NULL = loss only
-  const int64_t* target;  // [N]
+  Targets target;         // [N]
   int64_t N;
   int64_t V;
   int64_t ignore_index;
@@ -116,7 +116,7 @@ struct CeRowsParams {
   float* st;              // [N] target logit
   int32_t vectorized;     // rows start 16-byte aligned and V * elt % 16 == 0
 };
-cudaError_t launch_ce_count(const int64_t* target, int64_t N, int64_t V, int64_t ignore_index,
+cudaError_t launch_ce_count(Targets target, int64_t N, int64_t V, int64_t ignore_index,
                             Scalars* sc, int sms, cudaStream_t s);
 cudaError_t launch_ce_rows(const CeRowsParams& p, int elt, int sms, cudaStream_t s);
 

@@ -251,7 +251,7 @@ cudaError_t launch_transpose_f32(const float* in, int64_t R, int64_t C, int64_t 
 // Cross-entropy on materialised logits S [N, V] (bf16 or fp32).
 
 // n_valid (atomic integer adds: exact) and the bad-target flag.
-__global__ void ce_count_kernel(const int64_t* __restrict__ target, int64_t N, int64_t V,
+__global__ void ce_count_kernel(const Targets target, int64_t N, int64_t V,
                                 int64_t ignore_index, Scalars* sc) {
   int cnt = 0;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < N;
@@ -270,7 +270,7 @@ __global__ void ce_count_kernel(const int64_t* __restrict__ target, int64_t N, i
               static_cast<unsigned long long>(cnt));
 }
 
-cudaError_t launch_ce_count(const int64_t* target, int64_t N, int64_t V, int64_t ignore_index,
+cudaError_t launch_ce_count(Targets target, int64_t N, int64_t V, int64_t ignore_index,
                             Scalars* sc, int sms, cudaStream_t s) {
   int64_t blocks = (N + 255) / 256;
   if (blocks > static_cast<int64_t>(sms) * 4) blocks = static_cast<int64_t>(sms) * 4;

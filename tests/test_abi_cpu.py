@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_opts_layout_and_version(lib):
     import ctypes
     assert lib.flce_opts_sizeof() == ctypes.sizeof(flce.FlceOpts)
-    assert lib.flce_version() == 1
+    assert lib.flce_version() == 2
     o = flce.make_opts()
     assert o.sync == 1 and o.grad_scale == 1.0 and o.dtype == flce.FLCE_BF16
 

@@ -177,6 +177,47 @@ def test_shift_invariance_with_large_row_offsets(cuda_lib):
     assert_grad(dW.cpu().numpy(), ref["dW"], "dW")
 
 
+@pytest.mark.parametrize("N,H,V,dtype,vc", [
+    (513, 320, 3000, "bf16", 512),
+    (389, 100, 1300, "fp32", 768),
+])
+def test_int32_targets(cuda_lib, N, H, V, dtype, vc):
+    """target_is_int32: the ids given as int32 give bit for bit the results of
+    the same call with int64 ids (fused path, loss-only path, host-buffer
+    entry, CE on logits), the fused results match the oracle, and an int32
+    id outside [0, V) is reported as a bad target."""
+    X, W, t = make_case(N, H, V, dtype, seed=N + 31, ignore_num=10,
+                        w_std=0.05 if dtype == "bf16" else 0.1)
+    Xd, Wd, td = _gpu(X, W, t)
+    t32 = td.to(torch.int32)
+    a = cuda_lib.flce_fwd_bwd_ex(Xd, Wd, td, IGN, sync=True, vocab_chunk=vc)
+    b = cuda_lib.flce_fwd_bwd_ex(Xd, Wd, t32, IGN, sync=True, vocab_chunk=vc)
+    assert a[0].item() == b[0].item() and int(a[1].item()) == int(b[1].item())
+    assert torch.equal(a[2], b[2]) and torch.equal(a[3], b[3])
+    ref = oracle.flce(X, W, t, IGN)
+    assert int(b[1].item()) == ref["n_valid"]
+    assert_loss(b[0].item(), ref["loss"])
+    assert_grad(b[2].float().cpu().numpy(), ref["dX"], "dX")
+    assert_grad(b[3].cpu().numpy(), ref["dW"], "dW")
+    fa = cuda_lib.flce_fwd(Xd, Wd, td, IGN, sync=True)
+    fb = cuda_lib.flce_fwd(Xd, Wd, t32, IGN, sync=True)
+    assert fa[0].item() == fb[0].item()
+    loss_h, dX_h, dW_h = cuda_lib.flce_fwd_bwd_host(X.pin_memory(), W.pin_memory(),
+                                                    t.to(torch.int32).pin_memory(), IGN,
+                                                    vocab_chunk=vc)
+    assert loss_h == a[0].item()
+    assert torch.equal(dX_h, a[2].cpu()) and torch.equal(dW_h, a[3].cpu())
+    S = (Xd.float() @ Wd.float().t()).to(Xd.dtype).contiguous()
+    ca = cuda_lib.flce_ce_fwd_bwd(S, td, IGN, sync=True)
+    cb = cuda_lib.flce_ce_fwd_bwd(S, t32, IGN, sync=True)
+    assert ca[0].item() == cb[0].item() and torch.equal(ca[2], cb[2])
+    bad = t32.clone()
+    bad[N // 2] = V
+    with pytest.raises(cuda_lib.FlceError) as ei:
+        cuda_lib.flce_fwd_bwd_ex(Xd, Wd, bad, IGN, sync=True)
+    assert ei.value.status == cuda_lib.FLCE_ERR_TARGET
+
+
 def test_launch_sequence(cuda_lib):
     """Per-launch trace of a three-chunk call: pass 1, combine, then pass 2,
     dW and dX per chunk, then the bf16 conversion of dX."""

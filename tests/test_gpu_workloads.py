@@ -76,16 +76,19 @@ def _prefix_oracle(r, P):
     return r.cache[key]
 
 
+@pytest.fixture(scope="class")
+def run(request, cuda_lib):
+    """The full run of the requesting class's workload (class attribute NAME),
+    made once per class."""
+    r = _make_run(request.cls.NAME, cuda_lib)
+    yield r
+    r.__dict__.clear()
+    torch.cuda.empty_cache()
+
+
 class _EveryWorkload:
     """Checks made on every workload's full run."""
     NAME = None
-
-    @pytest.fixture(scope="class")
-    def run(self, cuda_lib):
-        r = _make_run(self.NAME, cuda_lib)
-        yield r
-        r.__dict__.clear()
-        torch.cuda.empty_cache()
 
     def test_count_loss_recheck_and_properties(self, run):
         """Count bit-exact; the loss and every row loss rechecked on the host
