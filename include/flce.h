@@ -237,6 +237,26 @@ FLCE_API size_t flce_opts_sizeof(void);
 FLCE_API int flce_selftest_wait_expiry(int64_t limit_ns);
 
 /*
+ * Scale and convert a gradient on the device, in one pass over memory:
+ *   dst[i] = (dst type)(src[i] * *scale_dev)   (bf16: round to nearest even)
+ * This is the step of `loss.backward()` after the overview's
+ * loss = loss_fn(weight, input, target) ("Método de API de Baixo Nível"): the
+ * gradients were computed in the forward call (dW fp32, dX in the input
+ * type), and the backward multiplies them by the incoming grad_output and
+ * casts dW to the weight's type.
+ *   src [n] of type src_dtype and dst [n] of type dst_dtype (FLCE_BF16 or
+ *   FLCE_FP32), device memory; dst may be src itself when the two types are
+ *   equal (in place); any other overlap is rejected.
+ *   scale_dev: device float (e.g. grad_output), or NULL for 1.
+ *   stream: cudaStream_t to launch on (NULL = legacy default stream).
+ * Asynchronous.  FLCE_ERR_ARG on n < 0, an unknown type, a null buffer with
+ * n > 0, or a forbidden overlap.
+ */
+FLCE_API int flce_scale_convert(const void* src, int32_t src_dtype, void* dst,
+                                int32_t dst_dtype, int64_t n, const float* scale_dev,
+                                void* stream);
+
+/*
  * Loss-only pass (the work of flce_fwd) that allocates no device memory.
  * The paper has no counterpart to this entry point; it exists for callers
  * that cannot call cudaMalloc at the point where the loss is needed: a host

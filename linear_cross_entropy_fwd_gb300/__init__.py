@@ -33,7 +33,7 @@ TRACE_KINDS = {1: "logits_lse", 2: "combine", 3: "logits_grad", 4: "dw", 5: "dx"
 EXPORTED = ["flce_opts_init", "flce_fwd_bwd", "flce_fwd_bwd_ex", "flce_fwd",
             "flce_fwd_bwd_host", "flce_workspace_bytes", "flce_status_str",
             "flce_last_error", "flce_version", "flce_opts_sizeof", "flce_fwd_noalloc",
-            "flce_ce_fwd_bwd", "flce_selftest_wait_expiry"]
+            "flce_ce_fwd_bwd", "flce_selftest_wait_expiry", "flce_scale_convert"]
 
 
 class FlceOpts(ctypes.Structure):
@@ -113,6 +113,8 @@ def load_library(path: str | None = None):
         lib.flce_ce_fwd_bwd.restype = i32
         lib.flce_selftest_wait_expiry.argtypes = [i64]
         lib.flce_selftest_wait_expiry.restype = i32
+        lib.flce_scale_convert.argtypes = [vp, i32, vp, i32, i64, vp, vp]
+        lib.flce_scale_convert.restype = i32
         if lib.flce_opts_sizeof() != ctypes.sizeof(FlceOpts):
             raise RuntimeError("flce_opts layout mismatch between libflce and the binding")
         _lib = lib
@@ -441,6 +443,29 @@ def flce_workspace_bytes(N: int, H: int, V: int, with_grads: bool = True,
     return int(lib.flce_workspace_bytes(N, H, V, 1 if with_grads else 0, ctypes.byref(o)))
 
 
+def scale_convert(src: torch.Tensor, dst: torch.Tensor,
+                  scale: torch.Tensor | None = None) -> torch.Tensor:
+    """dst = (dst.dtype)(src * scale) on the device in one pass (bf16 or
+    fp32 each; ``scale`` a one-element fp32 device tensor, None for 1).
+    ``dst`` may be ``src`` itself when the dtypes are equal.  Returns dst."""
+    lib = load_library()
+    if src.numel() != dst.numel() or not (src.is_contiguous() and dst.is_contiguous()):
+        raise ValueError("src and dst must be contiguous with the same number of elements")
+    if src.device != dst.device or not src.is_cuda:
+        raise ValueError("src and dst must be CUDA tensors on one device")
+    if scale is not None:
+        _check_out(scale, tuple(scale.shape), torch.float32, src.device, "scale")
+        if scale.numel() != 1:
+            raise ValueError("scale must hold one element")
+    with torch.cuda.device(src.device):
+        st = lib.flce_scale_convert(src.data_ptr(), _dtype_code(src), dst.data_ptr(),
+                                    _dtype_code(dst), src.numel(),
+                                    None if scale is None else scale.data_ptr(),
+                                    torch.cuda.current_stream(src.device).cuda_stream)
+    _check(st)
+    return dst
+
+
 class Trace:
     """Per-launch CUDA events recorded by the library on its stream."""
 
@@ -472,19 +497,28 @@ def _attach_trace(o: FlceOpts, trace: Trace | None):
     return (trace,)
 
 
+def _grad_scale(grad_out: torch.Tensor) -> torch.Tensor:
+    return grad_out.detach().to(torch.float32).reshape(1).contiguous()
+
+
 class _FLCEFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, weight, inp, target, ignore_index):
         loss, _, dX, dW = flce_fwd_bwd_ex(inp.contiguous(), weight.contiguous(),
                                           target.contiguous(), ignore_index)
         ctx.save_for_backward(dX, dW)
+        ctx.w_dtype = weight.dtype
         return loss
 
     @staticmethod
     def backward(ctx, grad_out):
+        # the gradients were computed in forward: scale them by grad_output
+        # (and cast dW to the weight's dtype) in the library, one pass each
         dX, dW = ctx.saved_tensors
-        gW = (dW * grad_out).to(dX.dtype) if dX.dtype != torch.float32 else dW * grad_out
-        return gW, dX * grad_out.to(dX.dtype), None, None
+        g = _grad_scale(grad_out)
+        gW = scale_convert(dW, torch.empty(dW.shape, dtype=ctx.w_dtype, device=dW.device), g)
+        gX = scale_convert(dX, torch.empty_like(dX), g)
+        return gW, gX, None, None
 
 
 class _CEFunction(torch.autograd.Function):
@@ -497,7 +531,7 @@ class _CEFunction(torch.autograd.Function):
     @staticmethod
     def backward(ctx, grad_out):
         (dS,) = ctx.saved_tensors
-        return dS * grad_out.to(dS.dtype), None, None
+        return scale_convert(dS, torch.empty_like(dS), _grad_scale(grad_out)), None, None
 
 
 class CrossEntropyLoss(torch.nn.Module):

@@ -416,15 +416,6 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
   const Targets tg{target, o.target_is_int32 != 0 ? 1 : 0};
   int rc;
   Tracer tr(o, s);
-  // GEMM launch k of this call takes its tiles from counter k % 3 and zeroes
-  // counter (k + 2) % 3 for the launch two later (the memset clears all three
-  // for the first two launches).
-  int n_gemm = 0;
-  auto schedule = [&](GemmGrid& g) {
-    g.tile_ctr = &sc->tile_ctr[n_gemm % 3];
-    g.ctr_reset = &sc->tile_ctr[(n_gemm + 2) % 3];
-    ++n_gemm;
-  };
 
   FLCE_CUDA(cudaMemsetAsync(sc, 0, sizeof(Scalars), s));
   if ((rc = tr.start())) return rc;
@@ -445,7 +436,6 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
       g.num_k_blk = static_cast<int32_t>((H + KE - 1) / KE);
       g.b_mn_off = static_cast<int32_t>(t0 * BN);
       g.status = &sc->status;
-      schedule(g);
       RowLseParams rp{tg, partial, st, N, V, static_cast<int32_t>(t0)};
       const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, units);
       FLCE_CUDA(bf16 ? launch_logits_lse_bf16(mX, mW, g, rp, grid, s)
@@ -523,7 +513,8 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
           g.num_k_blk = static_cast<int32_t>((H + KE - 1) / KE);
           g.b_mn_off = static_cast<int32_t>(c0);
           g.status = &sc->status;
-          schedule(g);  // operands are inputs; the epilogue waits before writing G
+          // operands are inputs: the loads start at once; the epilogue
+          // waits for the previous launch before it overwrites G
           GradLogitsParams gp{tg, lse2, sc, N, V, ignore_index, c0};
           const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, units);
           FLCE_CUDA(bf16 ? launch_logits_grad_bf16(mX_K, mW_K, mG_st, g, gp, grid, s)
@@ -545,7 +536,6 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
           g.status = &sc->status;
           g.raster_n = 1;  // a slab of G_c rows with all of X stays in L2
           g.wait_operands = 1;  // G_c comes from the launch just before
-          schedule(g);
           StoreParams sp{0, static_cast<int32_t>(c0), 0};
           const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, units);
           FLCE_CUDA(bf16 ? launch_dw_bf16(mA4, mB4, mdW, g, sp, grid, s)
@@ -570,7 +560,6 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
           g.status = &sc->status;
           // G_c comes from two launches back (the dW launch is in between),
           // so the operand loads start at once
-          schedule(g);
           StoreParams sp{0, 0, c > 0 ? 1 : 0};
           const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, units);
           FLCE_CUDA(bf16 ? launch_dx_bf16(mA5, mB5, mdX, g, sp, grid, s)
@@ -1036,6 +1025,32 @@ int flce_selftest_wait_expiry(int64_t limit_ns) {
   cudaFree(p);
   if (e != cudaSuccess) return cuda_fail(e, "wait-expiry self-test");
   return status_from_bits(h.status);
+}
+
+int flce_scale_convert(const void* src, int32_t src_dtype, void* dst, int32_t dst_dtype,
+                       int64_t n, const float* scale_dev, void* stream) {
+  g_last_error[0] = 0;
+  const bool ok_types = (src_dtype == FLCE_BF16 || src_dtype == FLCE_FP32) &&
+                        (dst_dtype == FLCE_BF16 || dst_dtype == FLCE_FP32);
+  if (n < 0 || !ok_types || (n > 0 && (!src || !dst))) {
+    set_error("flce_scale_convert: bad arguments (n >= 0, known types, non-null buffers)");
+    return FLCE_ERR_ARG;
+  }
+  const size_t se = src_dtype == FLCE_FP32 ? 4 : 2, de = dst_dtype == FLCE_FP32 ? 4 : 2;
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+  const uintptr_t s1 = s0 + static_cast<size_t>(n) * se, d1 = d0 + static_cast<size_t>(n) * de;
+  const bool in_place = (s0 == d0 && se == de);
+  if (n > 0 && !in_place && s0 < d1 && d0 < s1) {
+    set_error("flce_scale_convert: dst overlaps src (only an exact in-place call of one type "
+              "is allowed)");
+    return FLCE_ERR_ARG;
+  }
+  DeviceInfo D;
+  int rc = device_info(FLCE_BF16, &D);
+  if (rc) return rc;
+  FLCE_CUDA(launch_scale_convert(src, static_cast<int>(se), dst, static_cast<int>(de), n,
+                                 scale_dev, D.sms, static_cast<cudaStream_t>(stream)));
+  return FLCE_OK;
 }
 
 int flce_fwd_noalloc(const void* X, const void* W, const int64_t* target, int64_t N, int64_t H,

@@ -24,7 +24,6 @@ constexpr int STAGING_BUF_BYTES = 4096;              // one 32-row x 128-byte TM
 constexpr int STAGING_BYTES = EPI_WARPS * 2 * STAGING_BUF_BYTES;
 constexpr int TMEM_COLS = 2 * BN;                    // two fp32 accumulators of BN columns
 constexpr int SMEM_BARRIER_BYTES = 256;
-constexpr int SCHED_SLOTS = 4;                       // tile indices in flight per CTA
 constexpr int GEMM_SMEM_BYTES =
     1024 + STAGES * (A_STAGE_BYTES + B_STAGE_BYTES) + STAGING_BYTES + SMEM_BARRIER_BYTES;
 
@@ -43,8 +42,6 @@ struct GemmGrid {
   int32_t wait_operands;  // 1: an operand is written by the launch just before
                           // this one, so the loads wait for it to complete
   int32_t* status;     // device status word (FLCE_DEV_* bits)
-  uint32_t* tile_ctr;  // tile counter of this launch (zero at launch)
-  uint32_t* ctr_reset; // counter to zero for the launch two after this one
 };
 
 // Tile t of a launch -> (m block, n block).  The CTAs that run at the same
@@ -79,8 +76,6 @@ struct Scalars {
   float scale;        // grad_scale / normaliser (0 when nothing is valid)
   float loss;
   double loss_sum;
-  uint32_t tile_ctr[3];  // GEMM launch k takes its tiles from tile_ctr[k % 3]
-  uint32_t pad_;
 };
 
 }  // namespace flce

@@ -2,20 +2,18 @@
 //
 // D = A * B^T tile by tile, fp32 accumulation in TMEM, with a pluggable
 // epilogue that reads the accumulator straight out of TMEM (so logits never
-// travel to HBM).  Each scheduling unit (one CTA, or one CTA pair) takes tile
-// indices from a per-launch atomic counter, so the units that run together
-// hold consecutive tiles (the launch picks which tile index runs fastest,
-// tile_coords, so they share operands in L2), and a unit that starts early
-// takes more tiles than one that starts late.
+// travel to HBM).  Each scheduling unit (one CTA, or one CTA pair) walks the
+// tile space tile = unit + i * units; the launch picks which tile index runs
+// fastest (tile_coords) so the units that run together share tiles in L2.
 //
 // Launch overlap (programmatic dependent launch).  A launch's CTAs start as
 // the previous launch's CTAs leave their SMs.  The producer and the MMA
 // issuer start at once: they touch only operands written two or more
-// launches back (or, with wait_operands set, they first wait for the
-// previous launch).  The epilogue waits for the previous launch to complete
-// before its first global access, then lets the next launch start.  So when
-// a launch starts, the one two before it has completed, and its early units
-// fill the tail of the previous launch with their first tiles' MMAs.
+// launches back (or, with wait_operands set, the producer first waits for
+// the previous launch).  The epilogue waits for the previous launch to
+// complete before its first global access, then lets the next launch start.
+// So when a launch starts, the one two before it has completed, and its
+// early units run their first tiles' MMAs in the previous launch's tail.
 //
 // Two shapes of the engine:
 //   PAIR = false  one CTA per 128 x 256 tile (cta_group::1), 4-stage ring of
@@ -27,10 +25,7 @@
 //                 stages; half the B traffic per SM of the single-CTA shape.
 //
 // Roles (192 threads per CTA):
-//   warp 0      TMA producer; in the even (leader) CTA it also fetches the
-//               tile indices and publishes them, through a ring of
-//               SCHED_SLOTS entries in shared memory, to every role of both
-//               CTAs
+//   warp 0      TMA producer
 //   warp 1      TMEM allocator and MMA issuer (one thread of the even CTA),
 //               two accumulators of BN fp32 columns so the epilogue of tile i
 //               overlaps the MMAs of tile i+1
@@ -69,77 +64,9 @@ struct EngineShape {
   static constexpr uint32_t kABytes = BM * 128;
   static constexpr uint32_t kBBytes = kBRows * 128;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  // roles that take each published tile index: the MMA issuer and the
-  // epilogue warps of the leader, plus the producer and epilogue warps of
-  // the peer
-  static constexpr uint32_t kSchedTakers = PAIR ? 2 + 2 * EPI_WARPS : 1 + EPI_WARPS;
   static_assert(kStages * kStageBytes + STAGING_BYTES + SMEM_BARRIER_BYTES + 1024 <=
                     GEMM_SMEM_BYTES,
                 "shared memory plan");
-  // barriers, the TMEM address, the abort flag and the tile ring
-  static_assert((2 * kStages + 5 + 2 * SCHED_SLOTS) * 8 + 8 + 4 * SCHED_SLOTS <=
-                    SMEM_BARRIER_BYTES,
-                "barrier area");
-};
-
-// Tile index ring between the leader's producer and the other roles.  Entry
-// q of the sequence sits in slot q % SCHED_SLOTS of both CTAs; the leader's
-// sched_empty[slot] counts the takers.  An index >= the launch's tile count
-// ends the sequence.
-template <bool PAIR>
-struct TileRing {
-  uint64_t* full;      // [SCHED_SLOTS], this CTA's
-  uint64_t* empty;     // [SCHED_SLOTS], the leader's are used
-  volatile int* tile;  // [SCHED_SLOTS], this CTA's
-  volatile int* abort_flag;
-  int* status;
-
-  // Leader producer: publish the next entry to both CTAs.
-  __device__ __forceinline__ bool put(uint32_t& q, int value) const {
-    const uint32_t s = q % SCHED_SLOTS, r = q / SCHED_SLOTS;
-    if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, status)) return false;
-    tile[s] = value;
-    if (PAIR) {
-      st_shared_cluster_u32(mapa_shared(smem_addr(const_cast<int*>(&tile[s])), 1),
-                            static_cast<uint32_t>(value));
-      mbar_arrive_cluster(mapa_shared(smem_addr(&full[s]), 1));
-      mbar_arrive_cluster(mapa_shared(smem_addr(&full[s]), 0));
-    } else {
-      mbar_arrive(&full[s]);
-    }
-    ++q;
-    return true;
-  }
-
-  // One thread takes the next entry (and releases its slot).
-  __device__ __forceinline__ bool take(uint32_t& q, int& value) const {
-    const uint32_t s = q % SCHED_SLOTS, r = q / SCHED_SLOTS;
-    if (!mbar_wait<PAIR>(&full[s], r & 1, abort_flag, status)) return false;
-    value = tile[s];
-    release(s);
-    ++q;
-    return true;
-  }
-
-  // A whole warp takes the next entry; lane 0 releases the slot once every
-  // lane has read it.
-  __device__ __forceinline__ bool take_warp(uint32_t& q, int& value, int lane) const {
-    const uint32_t s = q % SCHED_SLOTS, r = q / SCHED_SLOTS;
-    const bool ok = mbar_wait<PAIR>(&full[s], r & 1, abort_flag, status);
-    if (!__all_sync(0xffffffffu, ok)) return false;
-    value = tile[s];
-    __syncwarp();
-    if (lane == 0) release(s);
-    ++q;
-    return true;
-  }
-
-  __device__ __forceinline__ void release(uint32_t s) const {
-    if (PAIR)
-      mbar_arrive_cluster(mapa_shared(smem_addr(&empty[s]), 0));
-    else
-      mbar_arrive(&empty[s]);
-  }
 };
 
 template <int ELT, bool A_MN, bool B_MN, bool PAIR, class Epi>
@@ -172,17 +99,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* acc_full = bars + 2 * STG;  // [2]
   uint64_t* acc_empty = acc_full + 2;   // [2]    (the even CTA's are the ones used)
   uint64_t* drain = acc_empty + 2;      // [1]
-  uint64_t* sched_full = drain + 1;     // [SCHED_SLOTS]
-  uint64_t* sched_empty = sched_full + SCHED_SLOTS;  // [SCHED_SLOTS] (the leader's are used)
-  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(sched_empty + SCHED_SLOTS);
+  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_slot + 1);
-  volatile int* sched_tile = abort_flag + 1;  // [SCHED_SLOTS]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int num_tiles = g.num_m_blk * g.num_n_blk;
-  const TileRing<PAIR> ring{sched_full, sched_empty, sched_tile, abort_flag, g.status};
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STG; ++s) {
@@ -194,10 +119,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&acc_empty[b], EPI_WARPS * S::kCtas);
     }
     mbar_init(drain, 1);
-    for (int s = 0; s < SCHED_SLOTS; ++s) {
-      mbar_init(&sched_full[s], 1);  // the leader's producer arrives on both CTAs' copies
-      mbar_init(&sched_empty[s], S::kSchedTakers);
-    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -228,31 +149,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t gk = 0, q = 0;
+      uint32_t gk = 0;
       bool ok = true;
       const uint64_t pol_a = l2_policy(g.a_l2);
       const uint64_t pol_b = l2_policy(g.b_l2);
-      // leader: tile indices from the launch's counter, one ahead
-      int next = 0;
-      if (rank == 0) next = static_cast<int>(atomicAdd(g.tile_ctr, 1u));
       if (g.wait_operands) grid_dependency_wait();
-      for (;;) {
-        int tile;
-        if (rank == 0) {
-          tile = next < num_tiles ? next : num_tiles;
-          if (!ring.put(q, tile)) {
-            ok = false;
-            break;
-          }
-          if (tile >= num_tiles) break;
-          next = static_cast<int>(atomicAdd(g.tile_ctr, 1u));
-        } else {
-          if (!ring.take(q, tile)) {
-            ok = false;
-            break;
-          }
-          if (tile >= num_tiles) break;
-        }
+      for (int tile = unit; ok && tile < num_tiles; tile += units) {
         int mu, n_blk;
         tile_coords(g, tile, mu, n_blk);
         const int m_blk = mu * S::kCtas + static_cast<int>(rank);
@@ -305,31 +207,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
         }
-        if (!ok) break;
       }
       // Drain: every stage this thread loaded must have landed before exit.
       // The even CTA sees its loads land on `full`; the odd CTA's loads land
       // on the even CTA's barrier, so it waits until the MMAs released them.
       const uint32_t n_drain = gk < STG ? gk : STG;
       for (uint32_t i = 0; i < n_drain; ++i) {
-        const uint32_t qq = gk - 1 - i;
+        const uint32_t q = gk - 1 - i;
         if (rank == 0)
-          mbar_wait_drain(&full[qq % STG], (qq / STG) & 1);
+          mbar_wait_drain(&full[q % STG], (q / STG) & 1);
         else
-          mbar_wait_drain(&empty[qq % STG], (qq / STG) & 1);
+          mbar_wait_drain(&empty[q % STG], (q / STG) & 1);
       }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0 && rank == 0) {
-      uint32_t gk = 0, q = 0;
+      uint32_t gk = 0, it = 0;
       bool ok = true;
       const uint32_t a_base = smem_addr(smA);
       const uint32_t b_base = smem_addr(smB);
-      for (uint32_t it = 0; ok; ++it) {
-        int tile;
-        if (!ring.take(q, tile)) break;
-        if (tile >= num_tiles) break;
+      for (int tile = unit; ok && tile < num_tiles; tile += units, ++it) {
         const uint32_t buf = it & 1;
         const uint32_t use = it >> 1;
         if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag, g.status)) {
@@ -383,15 +281,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ epilogue
     // The previous launch has completed before any epilogue reads or writes
     // global memory (and, through its own epilogue's wait, every launch
-    // before it).  Then this CTA lets the next launch start, and zeroes the
-    // tile counter of the launch after that (the launch that last used that
-    // counter, the previous one, is complete).
+    // before it).  Then this CTA lets the next launch start: its CTAs take
+    // SMs only as this launch's CTAs exit (the grid never has more units
+    // than fit at once).
     grid_dependency_wait();
-    if (warp == 2 && lane == 0) {
-      if (blockIdx.x == 0 && g.ctr_reset) *g.ctr_reset = 0u;
-      grid_launch_dependents();
-    }
-    const int q4 = warp & 3;  // TMEM lane quarter this warp may access
+    if (warp == 2 && lane == 0) grid_launch_dependents();
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
     uint8_t* stg = staging + (warp - 2) * 2 * STAGING_BUF_BYTES;
     uint32_t acc_empty_leader[2] = {0u, 0u};
     if (PAIR) {
@@ -400,11 +295,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     typename Epi::State st;
     Epi::init(st);
-    uint32_t q = 0;
-    for (uint32_t it = 0;; ++it) {
-      int tile;
-      if (!ring.take_warp(q, tile, lane)) break;
-      if (tile >= num_tiles) break;
+    uint32_t it = 0;
+    for (int tile = unit; tile < num_tiles; tile += units, ++it) {
       const uint32_t buf = it & 1;
       const uint32_t use = it >> 1;
       if (!mbar_wait(&acc_full[buf], use & 1, abort_flag, g.status)) break;
@@ -412,8 +304,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int mu, n_blk;
       tile_coords(g, tile, mu, n_blk);
       const int m_blk = mu * S::kCtas + static_cast<int>(rank);
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q4) << 16) + buf * BN;
-      Epi::tile(ep, st, &tmOut, taddr, m_blk, n_blk, q4, lane, stg);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * BN;
+      Epi::tile(ep, st, &tmOut, taddr, m_blk, n_blk, q, lane, stg);
       // every tcgen05.ld of this tile has completed (waited inside tile())
       tc_fence_before();
       __syncwarp();

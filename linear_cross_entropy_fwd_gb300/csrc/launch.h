@@ -123,4 +123,10 @@ cudaError_t launch_ce_rows(const CeRowsParams& p, int elt, int sms, cudaStream_t
 // fp32 [n] -> bf16 [n] (round to nearest even).
 cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t n, int sms, cudaStream_t s);
 
+// dst[i] = (dst type)(src[i] * *scale_dev) (scale 1 when scale_dev is NULL);
+// element sizes 2 (bf16) or 4 (fp32).  In place when dst == src and the
+// sizes are equal.
+cudaError_t launch_scale_convert(const void* src, int src_elt, void* dst, int dst_elt, int64_t n,
+                                 const float* scale_dev, int sms, cudaStream_t s);
+
 }  // namespace flce

@@ -65,36 +65,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Same with acquire semantics at cluster scope: the phase was completed by a
-// release at cluster scope from the peer CTA, and data the peer wrote into
-// this CTA's shared memory before that release is read after the wait.
-__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Wait until the phase with the given parity has completed.  Returns false on
 // timeout (limit_ns of %globaltimer) or when another role of this CTA has
-// already aborted.  CLUSTER selects the cluster-scope acquire.
-template <bool CLUSTER = false>
+// already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* status,
                                           uint64_t limit_ns = FLCE_WAIT_LIMIT_NS) {
   const uint32_t a = smem_addr(bar);
-  auto try_once = [a, parity]() {
-    return CLUSTER ? mbar_try_wait_acq_cluster(a, parity) : mbar_try_wait(a, parity);
-  };
-  if (try_once()) return true;
+  if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (try_once()) return true;
+    if (mbar_try_wait(a, parity)) return true;
     if ((it & 31) == 0) {
       if (*abort_flag) return false;
       if (global_timer_ns() - t0 > limit_ns) {
@@ -325,12 +306,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t cta_addr, uint32_t rank
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(cta_addr), "r"(rank));
   return r;
-}
-
-// 32-bit store to shared memory given by its shared::cluster address (may be
-// the peer CTA's).
-__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 // Arrive on an mbarrier given by its shared::cluster address (may be remote).

@@ -215,6 +215,80 @@ cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t n, int sms,
   return cudaGetLastError();
 }
 
+// dst = (dst type)(src * scale), 8 elements per thread and iteration when both
+// buffers are 16-byte aligned (the tail, or everything otherwise, one by one).
+template <int SE, int DE>
+__device__ __forceinline__ void load8(const void* src, int64_t k, float* f) {
+  if (SE == 4) {
+    const float4 a = __ldcs(static_cast<const float4*>(src) + 2 * k);
+    const float4 b = __ldcs(static_cast<const float4*>(src) + 2 * k + 1);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  } else {
+    const uint4 u = __ldcs(static_cast<const uint4*>(src) + k);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      f[2 * e] = __uint_as_float(w[e] << 16);
+      f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+  }
+}
+
+template <int SE, int DE>
+__global__ void scale_convert_kernel(const void* __restrict__ src, void* __restrict__ dst,
+                                     int64_t n, int vec, const float* __restrict__ scale_dev) {
+  const float sc = scale_dev ? *scale_dev : 1.f;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t n8 = vec ? n / 8 : 0;
+  for (int64_t k = tid; k < n8; k += stride) {
+    float f[8];
+    load8<SE, DE>(src, k, f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] *= sc;
+    if (DE == 4) {
+      __stcs(static_cast<float4*>(dst) + 2 * k, make_float4(f[0], f[1], f[2], f[3]));
+      __stcs(static_cast<float4*>(dst) + 2 * k + 1, make_float4(f[4], f[5], f[6], f[7]));
+    } else {
+      __stcs(static_cast<uint4*>(dst) + k,
+             make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                        pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7])));
+    }
+  }
+  for (int64_t i = n8 * 8 + tid; i < n; i += stride) {
+    const float x = (SE == 4 ? static_cast<const float*>(src)[i]
+                             : __uint_as_float(static_cast<uint32_t>(
+                                   static_cast<const uint16_t*>(src)[i]) << 16)) * sc;
+    if (DE == 4)
+      static_cast<float*>(dst)[i] = x;
+    else
+      static_cast<uint16_t*>(dst)[i] = static_cast<uint16_t>(pack_bf16x2(x, 0.f) & 0xFFFFu);
+  }
+}
+
+cudaError_t launch_scale_convert(const void* src, int src_elt, void* dst, int dst_elt, int64_t n,
+                                 const float* scale_dev, int sms, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int vec = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) ==
+                  0;
+  const int64_t work = vec ? (n + 7) / 8 : n;
+  int64_t blocks = (work + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  const dim3 grid(static_cast<unsigned>(blocks));
+  if (src_elt == 4 && dst_elt == 4)
+    scale_convert_kernel<4, 4><<<grid, 256, 0, s>>>(src, dst, n, vec, scale_dev);
+  else if (src_elt == 4)
+    scale_convert_kernel<4, 2><<<grid, 256, 0, s>>>(src, dst, n, vec, scale_dev);
+  else if (dst_elt == 4)
+    scale_convert_kernel<2, 4><<<grid, 256, 0, s>>>(src, dst, n, vec, scale_dev);
+  else
+    scale_convert_kernel<2, 2><<<grid, 256, 0, s>>>(src, dst, n, vec, scale_dev);
+  return cudaGetLastError();
+}
+
 // 32 x 32 tiles through shared memory (one padding column: no bank conflicts).
 __global__ void transpose_f32_kernel(const float* __restrict__ in, int64_t R, int64_t C,
                                      int64_t in_pitch, float* __restrict__ out,

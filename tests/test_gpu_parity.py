@@ -399,6 +399,40 @@ def test_autograd_module(cuda_lib):
     assert_grad(w.grad.float().cpu().numpy(), 3.0 * ref["dW"], "3 dW")
 
 
+@pytest.mark.parametrize("sdt,ddt", [(torch.float32, torch.bfloat16), (torch.float32, torch.float32),
+                                     (torch.bfloat16, torch.bfloat16),
+                                     (torch.bfloat16, torch.float32)])
+def test_scale_convert(cuda_lib, sdt, ddt):
+    """flce_scale_convert (the autograd backward's grad_output scaling and dW
+    cast): bit for bit the fp32 product rounded to the destination type, on
+    aligned buffers, on buffers one element off 16-byte alignment (the
+    element-by-element path), with a length that is not a multiple of 8,
+    without a scale, and in place."""
+    g = torch.Generator().manual_seed(3)
+    n = 100003
+    src = (torch.randn(n + 1, generator=g) * 5).to(sdt).to(DEV)
+    scale = torch.tensor([-0.3712], device=DEV)
+    for off in (0, 1):
+        a = src[off:off + n]
+        ref = (a.float() * scale).to(ddt)
+        out = torch.empty(n + 1, dtype=ddt, device=DEV)[off:off + n]
+        cuda_lib.scale_convert(a, out, scale)
+        assert torch.equal(out, ref)
+    out = torch.empty(n, dtype=ddt, device=DEV)
+    cuda_lib.scale_convert(src[:n], out)
+    assert torch.equal(out, src[:n].float().to(ddt))
+    if sdt == ddt:
+        buf = src[:n].clone()
+        cuda_lib.scale_convert(buf, buf, scale)
+        assert torch.equal(buf, (src[:n].float() * scale).to(ddt))
+    lib = cuda_lib.load_library()
+    codes = {torch.float32: cuda_lib.FLCE_FP32, torch.bfloat16: cuda_lib.FLCE_BF16}
+    base = torch.empty(64, dtype=torch.float32, device=DEV)
+    rc = lib.flce_scale_convert(base.data_ptr(), codes[torch.float32], base.data_ptr() + 8,
+                                codes[torch.float32], 32, None, None)
+    assert rc == cuda_lib.FLCE_ERR_ARG  # a shifted overlap is refused
+
+
 def test_caller_workspace(cuda_lib):
     X, W, t = make_case(300, 128, 2000, "bf16", seed=21, ignore_num=10)
     need = cuda_lib.flce_workspace_bytes(300, 128, 2000, True, vocab_chunk=512)
