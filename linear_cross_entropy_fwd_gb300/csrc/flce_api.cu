@@ -513,6 +513,10 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
           g.num_k_blk = static_cast<int32_t>((H + KE - 1) / KE);
           g.b_mn_off = static_cast<int32_t>(c0);
           g.status = &sc->status;
+          // N fastest: the chunk's W rows (Vc x H, 40 MB at the Llama-3 head)
+          // stay in L2 while X streams once (M fastest re-read X from DRAM:
+          // 332 against 121 MB per launch at 8192 x 4096, Vc 4864)
+          g.raster_n = 1;
           // operands are inputs: the loads start at once; the epilogue
           // waits for the previous launch before it overwrites G
           GradLogitsParams gp{tg, lse2, sc, N, V, ignore_index, c0};

@@ -178,6 +178,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
               for (int j = 0; j < BM / KE; ++j)
                 tma_load_2d_pair(&tmA, fb, a_dst + j * BOX_BYTES, a_mn + j * KE, ak);
+            } else if (g.a_l2) {
+              tma_load_2d_pair_hint(&tmA, fb, a_dst, ak, a_mn, pol_a);
             } else {
               tma_load_2d_pair(&tmA, fb, a_dst, ak, a_mn);
             }
@@ -185,6 +187,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
               for (int j = 0; j < S::kBRows / KE; ++j)
                 tma_load_2d_pair(&tmB, fb, b_dst + j * BOX_BYTES, b_mn + j * KE, bk);
+            } else if (g.b_l2) {
+              tma_load_2d_pair_hint(&tmB, fb, b_dst, bk, b_mn, pol_b);
             } else {
               tma_load_2d_pair(&tmB, fb, b_dst, bk, b_mn);
             }
