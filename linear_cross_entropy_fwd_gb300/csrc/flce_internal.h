@@ -37,6 +37,8 @@ struct GemmGrid {
   int32_t b_mn_off;
   int32_t b_k_off;
   int32_t raster_n;    // 0: M index fastest in the tile order, 1: N index fastest
+  int32_t m_band;      // raster_n = 0 and 0 < m_band < num_m_blk: the tile order
+                       // covers bands of m_band M blocks one after the other
   int32_t a_l2;        // L2 policy of operand loads: 0 normal, 1 evict first,
   int32_t b_l2;        // 2 evict last
   int32_t wait_operands;  // 1: an operand is written by the launch just before
@@ -47,11 +49,22 @@ struct GemmGrid {
 // Tile t of a launch -> (m block, n block).  The CTAs that run at the same
 // time cover a band of consecutive tiles: the fastest index sweeps its whole
 // operand, which should fit in L2 and stay resident, while the operand of
-// the slow index streams through once.
+// the slow index streams through once.  With m_band, M runs fastest inside
+// bands of m_band M blocks, and the bands follow one another: only one
+// band's rows of the M operand need to stay in L2, and the N operand streams
+// once per band.
 __host__ __device__ inline void tile_coords(const GemmGrid& g, int tile, int& m_blk, int& n_blk) {
   if (g.raster_n) {
     n_blk = tile % g.num_n_blk;
     m_blk = tile / g.num_n_blk;
+  } else if (g.m_band > 0 && g.m_band < g.num_m_blk) {
+    const int band_tiles = g.m_band * g.num_n_blk;
+    const int band = tile / band_tiles;
+    const int r = tile - band * band_tiles;
+    const int m0 = band * g.m_band;
+    const int rows = g.num_m_blk - m0 < g.m_band ? g.num_m_blk - m0 : g.m_band;
+    m_blk = m0 + r % rows;
+    n_blk = r / rows;
   } else {
     m_blk = tile % g.num_m_blk;
     n_blk = tile / g.num_m_blk;
