@@ -120,3 +120,47 @@ def test_header_is_plain_c(tmp_path, std, lang):
                         "-I", os.path.join(ROOT, "include"), str(src)],
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_tile_orders_cover_every_tile_once(tmp_path):
+    """The GEMM launches' tile orders (M fastest, N fastest, M fastest in
+    bands of M blocks, ragged last band) map the tile indices one to one
+    onto the tile grid: the engine's own tile_coords, compiled for the host."""
+    cxx = shutil.which("g++")
+    if cxx is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / "tiles.cpp"
+    src.write_text(r'''
+#include <cstdio>
+#include <vector>
+#define __host__
+#define __device__
+#include "flce_internal.h"
+int main() {
+  int bad = 0;
+  for (int nm : {1, 2, 5, 16, 17, 32, 64, 256})
+    for (int nn : {1, 3, 19, 501, 594})
+      for (int raster : {0, 1})
+        for (int band : {0, 1, 3, 8, 16, 18, 40}) {
+          flce::GemmGrid g{};
+          g.num_m_blk = nm; g.num_n_blk = nn; g.raster_n = raster; g.m_band = band;
+          std::vector<int> seen(nm * nn, 0);
+          for (int t = 0; t < nm * nn; ++t) {
+            int m, n;
+            flce::tile_coords(g, t, m, n);
+            if (m < 0 || m >= nm || n < 0 || n >= nn) { ++bad; continue; }
+            ++seen[m * nn + n];
+          }
+          for (int v : seen) bad += (v != 1);
+        }
+  std::printf("%d\n", bad);
+  return bad != 0;
+}
+''')
+    exe = tmp_path / "tiles"
+    csrc = os.path.join(ROOT, "linear_cross_entropy_fwd_gb300", "csrc")
+    r = subprocess.run([cxx, "-std=c++17", "-I", csrc, str(src), "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "0", r.stdout
