@@ -308,6 +308,17 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t cta_addr, uint32_t rank
   return r;
 }
 
+// Two floats from shared memory given by its shared::cluster address (may be
+// the peer CTA's).
+__device__ __forceinline__ float2 ld_shared_cluster_f2(uint32_t cluster_addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+               : "=f"(v.x), "=f"(v.y)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+
 // Arrive on an mbarrier given by its shared::cluster address (may be remote).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)

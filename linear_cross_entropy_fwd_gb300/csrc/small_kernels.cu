@@ -412,6 +412,19 @@ struct CeVec<4> {  // 4 fp32 per 16-byte access
 //         768 x 2 x 4 4.30, 1024 x 1 x 4 4.03, 768 x 1 x 6 3.80;
 //   fp32  1024 x 1 x 8 5.35, 1024 x 1 x 4 5.17, 512 x 1 x 8 4.89,
 //         512 x 2 x 4 4.73, 256 x 2 x 8 4.61.
+//
+// kSplit CTAs (a cluster) share each row of 16-byte vectors.  Split rows are
+// read from DRAM exactly once (8192 x 128256 bf16: 2.110 GB read for 2.10 GB
+// of logits, against 2.50 GB with one CTA per row), but every row then waits
+// on a cluster barrier.  Same-box sweep (TB/s of algorithmic bytes):
+//   bf16  split 1: 512 x 2 x 5 5.01;  split 2: 512 x 2 x 5 4.57,
+//         256 x 4 x 6 4.69, 256 x 4 x 8 4.13, 128 x 8 x 8 4.29;
+//         split 4: 256 x 4 x 6 2.92, 128 x 8 x 6 3.48;
+//   fp32  split 1: 1024 x 1 x 8 5.44;  split 2: 512 x 2 x 8 5.58,
+//         512 x 2 x 5 4.66, 256 x 4 x 4 4.77, 128 x 8 x 4 4.55;
+//         split 4: 256 x 4 x 6 4.14, 256 x 4 x 8 4.00.
+// A 256 KB bf16 row is too short to pay for the barrier; a 512 KB fp32 row
+// is not.
 template <int ELT>
 struct CeRowShape;
 template <>
@@ -419,20 +432,27 @@ struct CeRowShape<2> {
   static constexpr int kThreads = 512;
   static constexpr int kCtasPerSm = 2;
   static constexpr int kDepth = 5;
+  static constexpr int kSplit = 1;
 };
 template <>
 struct CeRowShape<4> {
-  static constexpr int kThreads = 1024;
-  static constexpr int kCtasPerSm = 1;
+  static constexpr int kThreads = 512;
+  static constexpr int kCtasPerSm = 2;
   static constexpr int kDepth = 8;
+  static constexpr int kSplit = 2;
 };
 
-// One CTA per row (grid-stride).  Pass A: max and sum of 2^(S log2 e) by an
-// online update per thread, merged across the CTA; lse2 and the target logit
-// go to the row-statistics buffers the combine kernel reads.  Pass B (when
-// dS is wanted): the row again (from L2: it was just read), and
-// dS = valid (2^(S log2 e - lse2) - [j = t]) * grad_scale / n.
-template <int ELT>
+// SPLIT CTAs per row (grid-stride over rows; SPLIT = 2 is a cluster of two
+// CTAs, each taking one half of every row's 16-byte vectors).  Pass A: max
+// and sum of 2^(S log2 e) by an online update per thread, merged across the
+// CTA and, with SPLIT = 2, with the peer CTA's half through distributed
+// shared memory (merged in rank order, so both CTAs hold the same lse); lse2
+// and the target logit go to the row-statistics buffers the combine kernel
+// reads.  Pass B (when dS is wanted): the CTA's part of the row again (from
+// L2: it was just read), and dS = valid (2^(S log2 e - lse2) - [j = t]) *
+// grad_scale / n.  Splitting a row halves the bytes each SM keeps pending in
+// L2 between a row's two reads.
+template <int ELT, int SPLIT>
 __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kCtasPerSm)
     ce_rows_kernel(const CeRowsParams p) {
   constexpr int kCeDepth = CeRowShape<ELT>::kDepth;
@@ -441,22 +461,30 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
   constexpr float kLog2e = 1.4426950408889634f;
   __shared__ float s_m[kThreads / 32], s_l[kThreads / 32];
   __shared__ float s_lse2;
+  __shared__ float2 s_half[2];  // this CTA's (max, sum) of its part of the row, by row parity
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool vec = p.vectorized;
+  const bool vec = SPLIT > 1 || p.vectorized;  // split rows are always vectorised
   const int64_t nvec = vec ? p.V / Vec::kPer : 0;
+  const uint32_t rank = SPLIT > 1 ? cluster_ctarank() : 0u;
+  const int64_t per_cta = (nvec + SPLIT - 1) / SPLIT;
+  const int64_t v_lo = rank * per_cta;                          // this CTA's vectors
+  const int64_t v_hi = v_lo + per_cta < nvec ? v_lo + per_cta : nvec;
+  const int64_t row0 = static_cast<int64_t>(blockIdx.x) / SPLIT;
+  const int64_t row_step = static_cast<int64_t>(gridDim.x) / SPLIT;
   const int64_t n = p.norm_count > 0 ? p.norm_count : p.sc->n_valid;
   const float scale = n > 0 ? static_cast<float>(static_cast<double>(p.grad_scale) /
                                                  static_cast<double>(n))
                             : 0.f;
   const uint64_t pol_keep = l2_policy(p.dlogits ? 2 : 1), pol_stream = l2_policy(1);
-  for (int64_t r = blockIdx.x; r < p.N; r += gridDim.x) {
+  int parity = 0;
+  for (int64_t r = row0; r < p.N; r += row_step, parity ^= 1) {
     const uint8_t* row = static_cast<const uint8_t*>(p.logits) + r * p.V * ELT;
     float m = -INFINITY, l = 0.f;
     if (vec) {
       // kCeDepth independent 16-byte loads in flight per thread
       const uint4* rv = reinterpret_cast<const uint4*>(row);
-      int64_t k = threadIdx.x;
-      for (; k + (kCeDepth - 1) * kThreads < nvec; k += kCeDepth * kThreads) {
+      int64_t k = v_lo + threadIdx.x;
+      for (; k + (kCeDepth - 1) * kThreads < v_hi; k += kCeDepth * kThreads) {
         uint4 u[kCeDepth];
 #pragma unroll
         for (int q = 0; q < kCeDepth; ++q)
@@ -481,7 +509,7 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
 #pragma unroll
           for (int e = 0; e < Vec::kPer; ++e) l += fast_exp2(fmaf(f[q][e], kLog2e, -m));
       }
-      for (; k < nvec; k += kThreads) {
+      for (; k < v_hi; k += kThreads) {
         float f[Vec::kPer];
         Vec::unpack(ld_nc_hint(rv + k, pol_keep), f);
 #pragma unroll
@@ -502,14 +530,42 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
       s_l[warp] = l;
     }
     __syncthreads();
+    float M = 0.f, L = 0.f;
     if (threadIdx.x == 0) {
-      float M = s_m[0], L = s_l[0];
+      M = s_m[0];
+      L = s_l[0];
       for (int w = 1; w < kThreads / 32; ++w) online_merge(M, L, s_m[w], s_l[w]);
+    }
+    if (SPLIT > 1) {
+      // swap the halves' statistics with the peer CTA; the slot alternates
+      // with the row, so the peer's read of this row's slot is ordered
+      // before this CTA rewrites it (two rows later) by the next row's
+      // cluster barrier
+      if (threadIdx.x == 0) s_half[parity] = make_float2(M, L);
+      cluster_sync();
+      if (threadIdx.x == 0) {
+        const uint32_t slot = smem_addr(&s_half[parity]);
+        const float2 h0 = ld_shared_cluster_f2(mapa_shared(slot, 0));
+        M = h0.x;
+        L = h0.y;
+#pragma unroll
+        for (int k = 1; k < SPLIT; ++k) {
+          const float2 hk = ld_shared_cluster_f2(mapa_shared(slot, static_cast<uint32_t>(k)));
+          online_merge(M, L, hk.x, hk.y);
+        }
+      }
+    }
+    if (threadIdx.x == 0) {
       const float lse2 = M + fast_log2(L);
       s_lse2 = lse2;
-      p.partial[r] = lse2;
+      if (rank == 0) p.partial[r] = lse2;
+      // the target logit, written by the CTA whose part holds it (rank 0
+      // writes 0 for an ignored or out-of-range target)
       const int64_t t = p.target[r];
-      p.st[r] = (t >= 0 && t < p.V) ? Vec::load1(row, t) : 0.f;
+      const bool in_row = (t >= 0 && t < p.V);
+      const uint32_t owner =
+          (SPLIT > 1 && in_row) ? static_cast<uint32_t>(t / Vec::kPer / per_cta) : 0u;
+      if (rank == owner) p.st[r] = in_row ? Vec::load1(row, t) : 0.f;
     }
     __syncthreads();
     if (p.dlogits) {
@@ -521,8 +577,8 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
       if (vec) {
         const uint4* rv = reinterpret_cast<const uint4*>(row);
         uint4* ov = reinterpret_cast<uint4*>(out);
-        int64_t k = threadIdx.x;
-        for (; k + (kCeDepth - 1) * kThreads < nvec; k += kCeDepth * kThreads) {
+        int64_t k = v_lo + threadIdx.x;
+        for (; k + (kCeDepth - 1) * kThreads < v_hi; k += kCeDepth * kThreads) {
           uint4 u[kCeDepth];
 #pragma unroll
           for (int q = 0; q < kCeDepth; ++q)
@@ -542,7 +598,7 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
             st_hint(ov + kk, Vec::pack(f), pol_stream);
           }
         }
-        for (; k < nvec; k += kThreads) {
+        for (; k < v_hi; k += kThreads) {
           float f[Vec::kPer];
           Vec::unpack(ld_hint(rv + k, pol_stream), f);
 #pragma unroll
@@ -566,17 +622,33 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
   }
 }
 
+template <int ELT, int SPLIT>
+cudaError_t launch_ce_rows_t(const CeRowsParams& p, int sms, cudaStream_t s) {
+  using Shape = CeRowShape<ELT>;
+  const int64_t cap = static_cast<int64_t>(sms) * Shape::kCtasPerSm / SPLIT;  // rows in flight
+  const int64_t rows = p.N < cap ? p.N : cap;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(static_cast<unsigned>(rows * SPLIT));
+  cfg.blockDim = dim3(Shape::kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = SPLIT;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ce_rows_kernel<ELT, SPLIT>, p);
+}
+
 cudaError_t launch_ce_rows(const CeRowsParams& p, int elt, int sms, cudaStream_t s) {
   if (p.N < 1) return cudaSuccess;
-  using Bf16 = CeRowShape<2>;
-  using F32 = CeRowShape<4>;
-  const int64_t cap = static_cast<int64_t>(sms) * (elt == 2 ? Bf16::kCtasPerSm : F32::kCtasPerSm);
-  const int64_t blocks = p.N < cap ? p.N : cap;
-  if (elt == 2)
-    ce_rows_kernel<2><<<static_cast<unsigned>(blocks), Bf16::kThreads, 0, s>>>(p);
-  else
-    ce_rows_kernel<4><<<static_cast<unsigned>(blocks), F32::kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  // rows of whole 16-byte vectors may be split across a cluster
+  if (p.vectorized)
+    return elt == 2 ? launch_ce_rows_t<2, CeRowShape<2>::kSplit>(p, sms, s)
+                    : launch_ce_rows_t<4, CeRowShape<4>::kSplit>(p, sms, s);
+  return elt == 2 ? launch_ce_rows_t<2, 1>(p, sms, s) : launch_ce_rows_t<4, 1>(p, sms, s);
 }
 
 }  // namespace flce
