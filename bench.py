@@ -141,10 +141,22 @@ class ClockSampler:
                 "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def kernel_source_hash() -> str:
+# The source files that make each kind of launch (its kernel code and the host
+# code that picks its tile order and launch shape).
+_GEMM_SOURCES = ["gemm.cuh", "epilogues.cuh", "sm103.cuh", "flce_internal.h",
+                 "gemm_instances.cuh", "gemm_bf16.cu", "launch.h", "flce_api.cu"]
+_SMALL_SOURCES = ["small_kernels.cu", "sm103.cuh", "flce_internal.h", "launch.h",
+                  "flce_api.cu"]
+KERNEL_SOURCES = {"logits_lse": _GEMM_SOURCES, "logits_grad": _GEMM_SOURCES,
+                  "dw": _GEMM_SOURCES, "dx": _GEMM_SOURCES, "combine": _SMALL_SOURCES,
+                  "convert": _SMALL_SOURCES, "ce_rows": _SMALL_SOURCES}
+
+
+def kernel_source_hash(kind: str) -> str:
+    """Hash of the sources a kind of launch is built from."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "linear_cross_entropy_fwd_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in sorted(KERNEL_SOURCES[kind]):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -152,14 +164,14 @@ def kernel_source_hash() -> str:
 
 def recorded_traffic(kind: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the current sources of that kind of launch (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(p):
+    if not os.path.exists(p) or kind not in KERNEL_SOURCES:
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(kind, {})
-    if e.get("source_hash") != kernel_source_hash() or e.get("workload") != workload:
+    if e.get("source_hash") != kernel_source_hash(kind) or e.get("workload") != workload:
         return None
     return e.get("dram_bytes_per_launch")
 
