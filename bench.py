@@ -360,6 +360,19 @@ def run_fwd(args, w):
     return 0
 
 
+def pinned_copy_rate(src, dst, reps: int = 3) -> float:
+    """Best-of-reps GB/s of one copy between pinned host and device memory."""
+    import torch
+    best = float("inf")
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        a = time.perf_counter()
+        dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        best = min(best, time.perf_counter() - a)
+    return src.numel() * src.element_size() / best / 1e9
+
+
 def workload_config(w, n_gpus):
     return {"workload": w.name, "N": w.N, "H": w.H, "V": w.V, "input_dtype": w.dtype,
             "ignored_rows": w.n_ignored, "targets": w.t_dist,
@@ -554,12 +567,17 @@ def main():
         dXh = torch.empty_like(Xh).pin_memory()
         dWh = torch.empty((V, H), dtype=torch.float32).pin_memory()
         flce.flce_fwd_bwd_host(Xh, Wh, th, w.ignore_index, dX=dXh, dW=dWh)
+        # the host link's rates just before the timed calls (context for e2e)
+        link = {"h2d_gbs": pinned_copy_rate(Wh, Wd), "d2h_gbs": pinned_copy_rate(dW, dWh)}
         if ws > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
+        per_call = []
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
+            a = time.perf_counter()
             flce.flce_fwd_bwd_host(Xh, Wh, th, w.ignore_index, dX=dXh, dW=dWh)
+            per_call.append(time.perf_counter() - a)  # the call is synchronous
         torch.cuda.synchronize(dev)
         e2e_s = (time.perf_counter() - t0) / args.e2e_steps
         e_t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
@@ -571,6 +589,8 @@ def main():
                        "d2h_bytes_per_step": dXh.numel() * dXh.element_size() +
                        dWh.numel() * 4 + 4,
                        "steps": args.e2e_steps,
+                       "ms_per_call": [round(1e3 * x, 3) for x in per_call],
+                       "host_link": link,
                        "timer": "host wall clock around synchronous calls"}
     if ws > 1:
         dist.barrier()
