@@ -10,8 +10,12 @@ then ``loss.backward()``, i.e. softmax cross-entropy on the LM-head logits
 with the exact gradients ("Cálculo Preciso").
 
 C names are kept: ``flce_fwd_bwd``, ``flce_fwd_bwd_ex``, ``flce_fwd``,
-``flce_fwd_bwd_host``, ``flce_workspace_bytes``.  ``LinearCrossEntropyLoss``
-is the autograd front with the overview's (weight, input, target) order.
+``flce_fwd_bwd_host``, ``flce_fwd_noalloc``, ``flce_ce_fwd_bwd``,
+``flce_workspace_bytes``; ``scale_convert`` wraps ``flce_scale_convert``.
+``LinearCrossEntropyLoss`` is the autograd front with the overview's
+(weight, input, target) order.  Every output buffer handed to the library
+is checked for shape, dtype, device and contiguity first, and each call runs
+with its input's device current.
 """
 from __future__ import annotations
 

@@ -164,3 +164,19 @@ int main() {
     assert r.returncode == 0, r.stderr
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0 and r.stdout.strip() == "0", r.stdout
+
+
+def test_binding_checks_output_buffers():
+    """The binding refuses an output buffer of the wrong shape, dtype or
+    layout before anything reaches the library (no device needed)."""
+    import torch
+    ok = torch.empty(5, dtype=torch.float32)
+    flce._check_out(ok, (5,), torch.float32, ok.device, "lse_out")
+    for bad in (torch.empty(4, dtype=torch.float32), torch.empty(5, dtype=torch.float64),
+                torch.empty(10, dtype=torch.float32)[::2]):
+        with pytest.raises(ValueError):
+            flce._check_out(bad, (5,), torch.float32, ok.device, "lse_out")
+    with pytest.raises(ValueError):
+        flce._check_row_outs(5, ok.device, torch.empty(6), None)
+    assert flce._is32(torch.zeros(3, dtype=torch.int32)) == 1
+    assert flce._is32(torch.zeros(3, dtype=torch.int64)) == 0
