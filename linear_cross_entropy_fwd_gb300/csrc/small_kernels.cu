@@ -427,12 +427,26 @@ struct CeVec<4> {  // 4 fp32 per 16-byte access
 // is not.
 template <int ELT>
 struct CeRowShape;
+//
+// kKeepBytes: the last bytes of a CTA's part of each row are also copied
+// into shared memory during the first pass, and the gradient pass reads them
+// from there: that part needs no second read from L2, and its first read is
+// marked evict-first.  Same-box A/B (TB/s): bf16 keep 0 4.81, 64 KB 4.96,
+// 96 KB 4.97; fp32 keep 0 5.35, 64 KB 5.31, 96 KB 5.48.  With 96 KB the bf16
+// kernel reads 2.18 GB from DRAM for 2.10 GB of logits (2.50 GB without).
+#ifndef FLCE_CE_KEEP_BF16
+#define FLCE_CE_KEEP_BF16 (96 * 1024)
+#endif
+#ifndef FLCE_CE_KEEP_FP32
+#define FLCE_CE_KEEP_FP32 (96 * 1024)
+#endif
 template <>
 struct CeRowShape<2> {
   static constexpr int kThreads = 512;
   static constexpr int kCtasPerSm = 2;
   static constexpr int kDepth = 5;
   static constexpr int kSplit = 1;
+  static constexpr int kKeepBytes = FLCE_CE_KEEP_BF16;
 };
 template <>
 struct CeRowShape<4> {
@@ -440,6 +454,7 @@ struct CeRowShape<4> {
   static constexpr int kCtasPerSm = 2;
   static constexpr int kDepth = 8;
   static constexpr int kSplit = 2;
+  static constexpr int kKeepBytes = FLCE_CE_KEEP_FP32;
 };
 
 // SPLIT CTAs per row (grid-stride over rows; SPLIT = 2 is a cluster of two
@@ -462,6 +477,8 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
   __shared__ float s_m[kThreads / 32], s_l[kThreads / 32];
   __shared__ float s_lse2;
   __shared__ float2 s_half[2];  // this CTA's (max, sum) of its part of the row, by row parity
+  extern __shared__ uint4 s_keep[];  // the kept tail of this CTA's part of the row
+  constexpr int64_t kKeepVecs = CeRowShape<ELT>::kKeepBytes / 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool vec = SPLIT > 1 || p.vectorized;  // split rows are always vectorised
   const int64_t nvec = vec ? p.V / Vec::kPer : 0;
@@ -469,6 +486,10 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
   const int64_t per_cta = (nvec + SPLIT - 1) / SPLIT;
   const int64_t v_lo = rank * per_cta;                          // this CTA's vectors
   const int64_t v_hi = v_lo + per_cta < nvec ? v_lo + per_cta : nvec;
+  // vectors [v_keep, v_hi) stay in shared memory between the two passes
+  // (only when there is a gradient pass and the rows are vectorised)
+  const int64_t v_keep =
+      (vec && p.dlogits) ? (v_hi - kKeepVecs > v_lo ? v_hi - kKeepVecs : v_lo) : v_hi;
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) / SPLIT;
   const int64_t row_step = static_cast<int64_t>(gridDim.x) / SPLIT;
   const int64_t n = p.norm_count > 0 ? p.norm_count : p.sc->n_valid;
@@ -487,8 +508,15 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
       for (; k + (kCeDepth - 1) * kThreads < v_hi; k += kCeDepth * kThreads) {
         uint4 u[kCeDepth];
 #pragma unroll
-        for (int q = 0; q < kCeDepth; ++q)
-          u[q] = ld_nc_hint(rv + k + q * kThreads, pol_keep);
+        for (int q = 0; q < kCeDepth; ++q) {
+          const int64_t kk = k + q * kThreads;
+          u[q] = ld_nc_hint(rv + kk, kk >= v_keep ? pol_stream : pol_keep);
+        }
+#pragma unroll
+        for (int q = 0; q < kCeDepth; ++q) {
+          const int64_t kk = k + q * kThreads;
+          if (kk >= v_keep) s_keep[kk - v_keep] = u[q];
+        }
         // the batch's max first: one rescale per batch, then one exp2 and one
         // add per element
         float f[kCeDepth][Vec::kPer];
@@ -511,7 +539,9 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
       }
       for (; k < v_hi; k += kThreads) {
         float f[Vec::kPer];
-        Vec::unpack(ld_nc_hint(rv + k, pol_keep), f);
+        const uint4 u = ld_nc_hint(rv + k, k >= v_keep ? pol_stream : pol_keep);
+        if (k >= v_keep) s_keep[k - v_keep] = u;
+        Vec::unpack(u, f);
 #pragma unroll
         for (int e = 0; e < Vec::kPer; ++e) online_add(m, l, f[e] * kLog2e);
       }
@@ -581,8 +611,10 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
         for (; k + (kCeDepth - 1) * kThreads < v_hi; k += kCeDepth * kThreads) {
           uint4 u[kCeDepth];
 #pragma unroll
-          for (int q = 0; q < kCeDepth; ++q)
-            u[q] = ld_hint(rv + k + q * kThreads, pol_stream);
+          for (int q = 0; q < kCeDepth; ++q) {
+            const int64_t kk = k + q * kThreads;
+            u[q] = kk >= v_keep ? s_keep[kk - v_keep] : ld_hint(rv + kk, pol_stream);
+          }
 #pragma unroll
           for (int q = 0; q < kCeDepth; ++q) {
             float f[Vec::kPer];
@@ -600,7 +632,7 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
         }
         for (; k < v_hi; k += kThreads) {
           float f[Vec::kPer];
-          Vec::unpack(ld_hint(rv + k, pol_stream), f);
+          Vec::unpack(k >= v_keep ? s_keep[k - v_keep] : ld_hint(rv + k, pol_stream), f);
 #pragma unroll
           for (int e = 0; e < Vec::kPer; ++e) {
             const int64_t j = k * Vec::kPer + e;
@@ -627,11 +659,17 @@ cudaError_t launch_ce_rows_t(const CeRowsParams& p, int sms, cudaStream_t s) {
   using Shape = CeRowShape<ELT>;
   const int64_t cap = static_cast<int64_t>(sms) * Shape::kCtasPerSm / SPLIT;  // rows in flight
   const int64_t rows = p.N < cap ? p.N : cap;
+  const int keep = (p.vectorized && p.dlogits) ? Shape::kKeepBytes : 0;
+  if (keep > 0) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        ce_rows_kernel<ELT, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, keep);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(static_cast<unsigned>(rows * SPLIT));
   cfg.blockDim = dim3(Shape::kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = static_cast<size_t>(keep);
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = SPLIT;
