@@ -149,7 +149,8 @@ _SMALL_SOURCES = ["small_kernels.cu", "sm103.cuh", "flce_internal.h", "launch.h"
                   "flce_api.cu"]
 KERNEL_SOURCES = {"logits_lse": _GEMM_SOURCES, "logits_grad": _GEMM_SOURCES,
                   "dw": _GEMM_SOURCES, "dx": _GEMM_SOURCES, "combine": _SMALL_SOURCES,
-                  "convert": _SMALL_SOURCES, "ce_rows": _SMALL_SOURCES}
+                  "convert": _SMALL_SOURCES, "ce_rows_bf16": _SMALL_SOURCES,
+                  "ce_rows_fp32": _SMALL_SOURCES}
 
 
 def kernel_source_hash(kind: str) -> str:
@@ -291,7 +292,7 @@ def run_ce_logits(args, w):
         "roofline": {"bound": "hbm", "kernel": "ce_rows", "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm,
                      "peak_kind": f"HBM copy ({peak_src})", "bytes_per_launch": algo_bytes,
-                     "traffic": recorded_traffic("ce_rows", w.name)},
+                     "traffic": recorded_traffic(f"ce_rows_{args.ce_dtype}", w.name)},
         "gpu_launches": 4 * args.steps, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

@@ -434,6 +434,13 @@ struct CeRowShape;
 // marked evict-first.  Same-box A/B (TB/s): bf16 keep 0 4.81, 64 KB 4.96,
 // 96 KB 4.97; fp32 keep 0 5.35, 64 KB 5.31, 96 KB 5.48.  With 96 KB the bf16
 // kernel reads 2.18 GB from DRAM for 2.10 GB of logits (2.50 GB without).
+// With the kept tail the loads in flight were swept again (same box, TB/s):
+//   bf16  split 1, 512 x 2: depth 3 4.88, 4 5.00, 5 4.96, 6 4.89;
+//         512 x 2 x 4 with 80 KB kept 4.97, 104 KB 4.68; 384 x 3 x 4 with
+//         64 KB 4.85; 256 x 4 x 6 with 48 KB 4.02;
+//   fp32  split 2, 512 x 2: depth 4 5.71, 5 5.97, 6 6.00, 7 5.91, 8 5.47,
+//         10 5.69; 512 x 2 x 6 with 80 KB kept 5.95; 256 x 4 x 8 with
+//         48 KB 4.05; split 1, 1024 x 1 x 8 with 192 KB 5.14.
 #ifndef FLCE_CE_KEEP_BF16
 #define FLCE_CE_KEEP_BF16 (96 * 1024)
 #endif
@@ -444,7 +451,7 @@ template <>
 struct CeRowShape<2> {
   static constexpr int kThreads = 512;
   static constexpr int kCtasPerSm = 2;
-  static constexpr int kDepth = 5;
+  static constexpr int kDepth = 4;
   static constexpr int kSplit = 1;
   static constexpr int kKeepBytes = FLCE_CE_KEEP_BF16;
 };
@@ -452,7 +459,7 @@ template <>
 struct CeRowShape<4> {
   static constexpr int kThreads = 512;
   static constexpr int kCtasPerSm = 2;
-  static constexpr int kDepth = 8;
+  static constexpr int kDepth = 6;
   static constexpr int kSplit = 2;
   static constexpr int kKeepBytes = FLCE_CE_KEEP_FP32;
 };
