@@ -755,7 +755,7 @@ int ce_entry(const void* logits, const int64_t* target, int64_t N, int64_t V,
     cp.st = reinterpret_cast<float*>(ws + off_st);
     cp.vectorized = ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(dlogits)) &
                      15u) == 0 &&
-                    (V * elt) % 16 == 0;
+                    (V * elt) % 16 == 0 && (V * elt) / 16 < (int64_t{1} << 30);
     e = launch_ce_rows(cp, elt, D.sms, s);
     if (e != cudaSuccess) rc = cuda_fail(e, "ce_rows");
     if (rc == FLCE_OK) rc = tr.after(FLCE_TRACE_CE_ROWS);

@@ -114,7 +114,7 @@ struct CeRowsParams {
   int64_t norm_count;
   float* partial;         // [N] lse2 per row (the combine's single statistic)
   float* st;              // [N] target logit
-  int32_t vectorized;     // rows start 16-byte aligned and V * elt % 16 == 0
+  int32_t vectorized;     // rows start 16-byte aligned, V * elt % 16 == 0, < 2^30 vectors
 };
 cudaError_t launch_ce_count(Targets target, int64_t N, int64_t V, int64_t ignore_index,
                             Scalars* sc, int sms, cudaStream_t s);

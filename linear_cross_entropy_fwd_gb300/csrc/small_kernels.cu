@@ -22,7 +22,7 @@ __device__ __forceinline__ void online_add(float& m, float& l, float u) {
   if (u > m) {
     l = l * fast_exp2(m - u) + 1.f;
     m = u;
-  } else {
+  } else if (u != -INFINITY) {  // a masked (-inf) logit adds nothing, even while m is -inf
     l += fast_exp2(u - m);
   }
 }
@@ -441,6 +441,10 @@ struct CeRowShape;
 //   fp32  split 2, 512 x 2: depth 4 5.71, 5 5.97, 6 6.00, 7 5.91, 8 5.47,
 //         10 5.69; 512 x 2 x 6 with 80 KB kept 5.95; 256 x 4 x 8 with
 //         48 KB 4.05; split 1, 1024 x 1 x 8 with 192 KB 5.14.
+// With the gradient pass cut to one comparison per vector for the target and
+// the scale folded into the exponent (about half the instructions per
+// logit), once more: bf16 512 x 2 depth 3 5.68, 4 5.87, 5 5.97, 6 5.55;
+// fp32 split 2, 512 x 2 depth 4 5.90, 5 6.06, 6 6.02, 8 5.97.
 #ifndef FLCE_CE_KEEP_BF16
 #define FLCE_CE_KEEP_BF16 (96 * 1024)
 #endif
@@ -451,7 +455,7 @@ template <>
 struct CeRowShape<2> {
   static constexpr int kThreads = 512;
   static constexpr int kCtasPerSm = 2;
-  static constexpr int kDepth = 4;
+  static constexpr int kDepth = 5;
   static constexpr int kSplit = 1;
   static constexpr int kKeepBytes = FLCE_CE_KEEP_BF16;
 };
@@ -459,25 +463,147 @@ template <>
 struct CeRowShape<4> {
   static constexpr int kThreads = 512;
   static constexpr int kCtasPerSm = 2;
-  static constexpr int kDepth = 6;
+  static constexpr int kDepth = 5;
   static constexpr int kSplit = 2;
   static constexpr int kKeepBytes = FLCE_CE_KEEP_FP32;
 };
 
+// Pass A over one CTA's vectors k, k + T, ... below hi of a row: (m, l) in the
+// log2 domain, kDepth 16-byte loads in flight per thread.  With KEEP each
+// vector read is also copied to keep[kk - keep_off].
+// Folds NV 16-byte vectors into (m, l): the vectors' max first, so one
+// rescale per call and then one exp2 and one add per element.
+template <int ELT, int NV>
+__device__ __forceinline__ void ce_stats_add(const uint4 (&u)[NV], float& m, float& l) {
+  using Vec = CeVec<ELT>;
+  constexpr float kLog2e = 1.4426950408889634f;
+  float f[NV][Vec::kPer];
+  float bmax = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < NV; ++q) {
+    Vec::unpack(u[q], f[q]);
+#pragma unroll
+    for (int e = 0; e < Vec::kPer; ++e) bmax = fmaxf(bmax, f[q][e]);
+  }
+  const float um = bmax * kLog2e;
+  if (um > m) {
+    l *= fast_exp2(m - um);  // m = -inf: l is 0 and stays 0
+    m = um;
+  }
+  // while every logit so far is -inf (masked), m is -inf and each term is 0
+  const float sub = m == -INFINITY ? 0.f : m;
+#pragma unroll
+  for (int q = 0; q < NV; ++q)
+#pragma unroll
+    for (int e = 0; e < Vec::kPer; ++e) l += fast_exp2(fmaf(f[q][e], kLog2e, -sub));
+}
+
+// Pass A over one CTA's vectors k, k + T, ... below hi of a row: (m, l) in the
+// log2 domain, kDepth 16-byte loads in flight per thread.  With KEEP each
+// vector read is also copied to keep[kk - keep_off].
+template <int ELT, bool KEEP>
+__device__ __forceinline__ void ce_stats_vectors(const uint4* rv, int k, int hi, uint64_t pol,
+                                                 uint4* keep, int keep_off, float& m, float& l) {
+  constexpr int D = CeRowShape<ELT>::kDepth, T = CeRowShape<ELT>::kThreads;
+  for (; k + (D - 1) * T < hi; k += D * T) {
+    uint4 u[D];
+#pragma unroll
+    for (int q = 0; q < D; ++q) u[q] = ld_nc_hint(rv + k + q * T, pol);
+    if (KEEP) {
+#pragma unroll
+      for (int q = 0; q < D; ++q) keep[k + q * T - keep_off] = u[q];
+    }
+    ce_stats_add<ELT, D>(u, m, l);
+  }
+  for (; k < hi; k += T) {
+    const uint4 u[1] = {ld_nc_hint(rv + k, pol)};
+    if (KEEP) keep[k - keep_off] = u[0];
+    ce_stats_add<ELT, 1>(u, m, l);
+  }
+}
+
+// dS of one 16-byte vector: 2^(S log2 e - c) for every element, the target's
+// element (te of vector tv) less `one`, then (unless FOLD) times sc.  With
+// FOLD, c already holds lse2 - log2 sc and `one` is sc.
+template <int ELT, bool FOLD>
+__device__ __forceinline__ uint4 ce_grad_vector(const uint4& u, int kk, float c, float sc,
+                                                float one, int tv, int te) {
+  using Vec = CeVec<ELT>;
+  constexpr float kLog2e = 1.4426950408889634f;
+  float f[Vec::kPer];
+  Vec::unpack(u, f);
+#pragma unroll
+  for (int e = 0; e < Vec::kPer; ++e) f[e] = fast_exp2(fmaf(f[e], kLog2e, -c));
+  if (kk == tv) {  // one vector per row
+#pragma unroll
+    for (int e = 0; e < Vec::kPer; ++e)
+      if (e == te) f[e] -= one;
+  }
+  if (!FOLD) {
+#pragma unroll
+    for (int e = 0; e < Vec::kPer; ++e) f[e] *= sc;
+  }
+  return Vec::pack(f);
+}
+
+// Pass B over one CTA's vectors k, k + T, ... below hi of a row: read from
+// global memory (an L2 hit: the row was just read), or from keep[kk -
+// keep_off] where pass A copied them; dS written to ov.  rv and ov may be the
+// same row (in place): each thread reads a vector before it writes it.
+template <int ELT, bool FROM_KEEP, bool FOLD>
+__device__ __forceinline__ void ce_grad_vectors(const uint4* rv, uint4* ov, int k, int hi,
+                                                const uint4* keep, int keep_off, uint64_t pol,
+                                                float c, float sc, float one, int tv, int te) {
+  constexpr int D = CeRowShape<ELT>::kDepth, T = CeRowShape<ELT>::kThreads;
+  for (; k + (D - 1) * T < hi; k += D * T) {
+    uint4 u[D];
+#pragma unroll
+    for (int q = 0; q < D; ++q)
+      u[q] = FROM_KEEP ? keep[k + q * T - keep_off] : ld_hint(rv + k + q * T, pol);
+#pragma unroll
+    for (int q = 0; q < D; ++q)
+      st_hint(ov + k + q * T, ce_grad_vector<ELT, FOLD>(u[q], k + q * T, c, sc, one, tv, te),
+              pol);
+  }
+  for (; k < hi; k += T) {
+    const uint4 u = FROM_KEEP ? keep[k - keep_off] : ld_hint(rv + k, pol);
+    st_hint(ov + k, ce_grad_vector<ELT, FOLD>(u, k, c, sc, one, tv, te), pol);
+  }
+}
+
+template <int ELT, bool FOLD>
+__device__ __forceinline__ void ce_grad_row(const uint4* rv, uint4* ov, int v_lo, int v_keep,
+                                            int v_hi, const uint4* keep, uint64_t pol, float c,
+                                            float sc, float one, int tv, int te) {
+  ce_grad_vectors<ELT, false, FOLD>(rv, ov, v_lo + static_cast<int>(threadIdx.x), v_keep, keep,
+                                    0, pol, c, sc, one, tv, te);
+  ce_grad_vectors<ELT, true, FOLD>(rv, ov, v_keep + static_cast<int>(threadIdx.x), v_hi, keep,
+                                   v_keep, pol, c, sc, one, tv, te);
+}
+
 // SPLIT CTAs per row (grid-stride over rows; SPLIT = 2 is a cluster of two
 // CTAs, each taking one half of every row's 16-byte vectors).  Pass A: max
-// and sum of 2^(S log2 e) by an online update per thread, merged across the
-// CTA and, with SPLIT = 2, with the peer CTA's half through distributed
-// shared memory (merged in rank order, so both CTAs hold the same lse); lse2
-// and the target logit go to the row-statistics buffers the combine kernel
-// reads.  Pass B (when dS is wanted): the CTA's part of the row again (from
-// L2: it was just read), and dS = valid (2^(S log2 e - lse2) - [j = t]) *
-// grad_scale / n.  Splitting a row halves the bytes each SM keeps pending in
-// L2 between a row's two reads.
+// and sum of 2^(S log2 e) per thread, merged across the CTA and, with SPLIT
+// = 2, with the peer CTA's half through distributed shared memory (merged in
+// rank order, so both CTAs hold the same lse); lse2 and the target logit go
+// to the row-statistics buffers the combine kernel reads.  Pass B (when dS is
+// wanted): the CTA's part of the row again, and dS = (2^(S log2 e - lse2) -
+// [j = t]) * grad_scale / n, zero on a row whose target is ignored.
+// Splitting a row halves the bytes each SM keeps pending in L2 between a
+// row's two reads.
+//
+// On the vector path each row's part is two ranges: [v_lo, v_keep), read
+// from global memory in both passes, and [v_keep, v_hi), at most kKeepBytes,
+// which pass A also copies to shared memory and pass B reads from there.
+// v_keep - v_lo is a whole number of passes of the CTA (kThreads vectors), so
+// each thread's vectors continue from one range into the next, and neither
+// range tests a vector's position against v_keep.  With a positive
+// scale sc, pass B computes 2^(S log2 e - (lse2 - log2 sc)) instead of
+// multiplying by sc, and corrects the target's element by -sc: the one
+// vector of the row that holds it is found by one comparison per vector.
 template <int ELT, int SPLIT>
 __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kCtasPerSm)
     ce_rows_kernel(const CeRowsParams p) {
-  constexpr int kCeDepth = CeRowShape<ELT>::kDepth;
   constexpr int kThreads = CeRowShape<ELT>::kThreads;
   using Vec = CeVec<ELT>;
   constexpr float kLog2e = 1.4426950408889634f;
@@ -485,73 +611,42 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
   __shared__ float s_lse2;
   __shared__ float2 s_half[2];  // this CTA's (max, sum) of its part of the row, by row parity
   extern __shared__ uint4 s_keep[];  // the kept tail of this CTA's part of the row
-  constexpr int64_t kKeepVecs = CeRowShape<ELT>::kKeepBytes / 16;
+  constexpr int kKeepVecs = CeRowShape<ELT>::kKeepBytes / 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = static_cast<int>(threadIdx.x);
   const bool vec = SPLIT > 1 || p.vectorized;  // split rows are always vectorised
-  const int64_t nvec = vec ? p.V / Vec::kPer : 0;
-  const uint32_t rank = SPLIT > 1 ? cluster_ctarank() : 0u;
-  const int64_t per_cta = (nvec + SPLIT - 1) / SPLIT;
-  const int64_t v_lo = rank * per_cta;                          // this CTA's vectors
-  const int64_t v_hi = v_lo + per_cta < nvec ? v_lo + per_cta : nvec;
+  // vector indices within a row fit in an int: the host vectorises only rows
+  // of fewer than 2^30 vectors
+  const int nvec = vec ? static_cast<int>(p.V / Vec::kPer) : 0;
+  const int rank = SPLIT > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int per_cta = (nvec + SPLIT - 1) / SPLIT;
+  const int v_lo = rank * per_cta < nvec ? rank * per_cta : nvec;  // this CTA's vectors
+  const int v_hi = v_lo + per_cta < nvec ? v_lo + per_cta : nvec;
   // vectors [v_keep, v_hi) stay in shared memory between the two passes
   // (only when there is a gradient pass and the rows are vectorised)
-  const int64_t v_keep =
-      (vec && p.dlogits) ? (v_hi - kKeepVecs > v_lo ? v_hi - kKeepVecs : v_lo) : v_hi;
+  int v_keep = v_hi;
+  if (vec && p.dlogits) {
+    const int over = v_hi - v_lo - kKeepVecs;
+    const int skip = over > 0 ? (over + kThreads - 1) / kThreads * kThreads : 0;
+    v_keep = v_lo + skip < v_hi ? v_lo + skip : v_hi;
+  }
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) / SPLIT;
   const int64_t row_step = static_cast<int64_t>(gridDim.x) / SPLIT;
   const int64_t n = p.norm_count > 0 ? p.norm_count : p.sc->n_valid;
   const float scale = n > 0 ? static_cast<float>(static_cast<double>(p.grad_scale) /
                                                  static_cast<double>(n))
                             : 0.f;
+  const bool fold = scale > 0.f;
+  const float log2_scale = fold ? log2f(scale) : 0.f;
   const uint64_t pol_keep = l2_policy(p.dlogits ? 2 : 1), pol_stream = l2_policy(1);
   int parity = 0;
   for (int64_t r = row0; r < p.N; r += row_step, parity ^= 1) {
     const uint8_t* row = static_cast<const uint8_t*>(p.logits) + r * p.V * ELT;
     float m = -INFINITY, l = 0.f;
     if (vec) {
-      // kCeDepth independent 16-byte loads in flight per thread
       const uint4* rv = reinterpret_cast<const uint4*>(row);
-      int64_t k = v_lo + threadIdx.x;
-      for (; k + (kCeDepth - 1) * kThreads < v_hi; k += kCeDepth * kThreads) {
-        uint4 u[kCeDepth];
-#pragma unroll
-        for (int q = 0; q < kCeDepth; ++q) {
-          const int64_t kk = k + q * kThreads;
-          u[q] = ld_nc_hint(rv + kk, kk >= v_keep ? pol_stream : pol_keep);
-        }
-#pragma unroll
-        for (int q = 0; q < kCeDepth; ++q) {
-          const int64_t kk = k + q * kThreads;
-          if (kk >= v_keep) s_keep[kk - v_keep] = u[q];
-        }
-        // the batch's max first: one rescale per batch, then one exp2 and one
-        // add per element
-        float f[kCeDepth][Vec::kPer];
-        float bmax = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < kCeDepth; ++q) {
-          Vec::unpack(u[q], f[q]);
-#pragma unroll
-          for (int e = 0; e < Vec::kPer; ++e) bmax = fmaxf(bmax, f[q][e]);
-        }
-        const float um = bmax * kLog2e;
-        if (um > m) {
-          l *= fast_exp2(m - um);  // m = -inf: l is 0 and stays 0
-          m = um;
-        }
-#pragma unroll
-        for (int q = 0; q < kCeDepth; ++q)
-#pragma unroll
-          for (int e = 0; e < Vec::kPer; ++e) l += fast_exp2(fmaf(f[q][e], kLog2e, -m));
-      }
-      for (; k < v_hi; k += kThreads) {
-        float f[Vec::kPer];
-        const uint4 u = ld_nc_hint(rv + k, k >= v_keep ? pol_stream : pol_keep);
-        if (k >= v_keep) s_keep[k - v_keep] = u;
-        Vec::unpack(u, f);
-#pragma unroll
-        for (int e = 0; e < Vec::kPer; ++e) online_add(m, l, f[e] * kLog2e);
-      }
+      ce_stats_vectors<ELT, false>(rv, v_lo + tid, v_keep, pol_keep, s_keep, 0, m, l);
+      ce_stats_vectors<ELT, true>(rv, v_keep + tid, v_hi, pol_stream, s_keep, v_keep, m, l);
     } else {
       for (int64_t j = threadIdx.x; j < p.V; j += kThreads)
         online_add(m, l, Vec::load1(row, j) * kLog2e);
@@ -600,8 +695,7 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
       // writes 0 for an ignored or out-of-range target)
       const int64_t t = p.target[r];
       const bool in_row = (t >= 0 && t < p.V);
-      const uint32_t owner =
-          (SPLIT > 1 && in_row) ? static_cast<uint32_t>(t / Vec::kPer / per_cta) : 0u;
+      const int owner = (SPLIT > 1 && in_row) ? static_cast<int>(t / Vec::kPer / per_cta) : 0;
       if (rank == owner) p.st[r] = in_row ? Vec::load1(row, t) : 0.f;
     }
     __syncthreads();
@@ -609,46 +703,25 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
       const float lse2 = s_lse2;
       const int64_t t = p.target[r];
       const bool valid = (t != p.ignore_index) && t >= 0 && t < p.V;
-      const float sc = valid ? scale : 0.f;
       uint8_t* out = static_cast<uint8_t*>(p.dlogits) + r * p.V * ELT;
       if (vec) {
         const uint4* rv = reinterpret_cast<const uint4*>(row);
         uint4* ov = reinterpret_cast<uint4*>(out);
-        int64_t k = v_lo + threadIdx.x;
-        for (; k + (kCeDepth - 1) * kThreads < v_hi; k += kCeDepth * kThreads) {
-          uint4 u[kCeDepth];
-#pragma unroll
-          for (int q = 0; q < kCeDepth; ++q) {
-            const int64_t kk = k + q * kThreads;
-            u[q] = kk >= v_keep ? s_keep[kk - v_keep] : ld_hint(rv + kk, pol_stream);
-          }
-#pragma unroll
-          for (int q = 0; q < kCeDepth; ++q) {
-            float f[Vec::kPer];
-            Vec::unpack(u[q], f);
-            const int64_t kk = k + q * kThreads;
-            // the target's position inside this vector, or -1
-            const int64_t d = t - kk * Vec::kPer;
-            const int tl = (d >= 0 && d < Vec::kPer) ? static_cast<int>(d) : -1;
-#pragma unroll
-            for (int e = 0; e < Vec::kPer; ++e)
-              f[e] = valid ? (fast_exp2(fmaf(f[e], kLog2e, -lse2)) - (e == tl ? 1.f : 0.f)) * sc
-                           : 0.f;
-            st_hint(ov + kk, Vec::pack(f), pol_stream);
-          }
-        }
-        for (; k < v_hi; k += kThreads) {
-          float f[Vec::kPer];
-          Vec::unpack(k >= v_keep ? s_keep[k - v_keep] : ld_hint(rv + k, pol_stream), f);
-#pragma unroll
-          for (int e = 0; e < Vec::kPer; ++e) {
-            const int64_t j = k * Vec::kPer + e;
-            f[e] = valid ? (fast_exp2(fmaf(f[e], kLog2e, -lse2)) - (j == t ? 1.f : 0.f)) * sc
-                         : 0.f;
-          }
-          st_hint(ov + k, Vec::pack(f), pol_stream);
+        if (!valid) {
+          for (int k = v_lo + tid; k < v_hi; k += kThreads)
+            st_hint(ov + k, make_uint4(0u, 0u, 0u, 0u), pol_stream);
+        } else {
+          const int tv = static_cast<int>(t / Vec::kPer);
+          const int te = static_cast<int>(t - static_cast<int64_t>(tv) * Vec::kPer);
+          if (fold)
+            ce_grad_row<ELT, true>(rv, ov, v_lo, v_keep, v_hi, s_keep, pol_stream,
+                                   lse2 - log2_scale, scale, scale, tv, te);
+          else
+            ce_grad_row<ELT, false>(rv, ov, v_lo, v_keep, v_hi, s_keep, pol_stream, lse2, scale,
+                                    1.f, tv, te);
         }
       } else {
+        const float sc = valid ? scale : 0.f;
         for (int64_t j = threadIdx.x; j < p.V; j += kThreads) {
           const float x = Vec::load1(row, j);
           const float g =
@@ -657,7 +730,7 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
         }
       }
     }
-    __syncthreads();  // s_m / s_l / s_lse2 are reused by the next row
+    __syncthreads();  // s_m / s_l / s_lse2 / s_keep are reused by the next row
   }
 }
 

@@ -52,6 +52,39 @@ def test_ce_matches_oracle(cuda_lib, N, V, dtype, ign):
     assert_grad(dS.float().cpu().numpy(), ref["dS"], "dS")
 
 
+@pytest.mark.parametrize("N,V,dtype", [
+    (64, 32000, "bf16"),    # vector path, one CTA per row
+    (40, 60000, "fp32"),    # vector path, rows split across a cluster
+    (50, 777, "bf16"),      # scalar path
+])
+def test_ce_masked_logits(cuda_lib, N, V, dtype):
+    """-inf (masked) logits: a long run at the start of even rows, so that
+    whole batches a thread reads first are masked, and every 7th column of odd
+    rows.  Masked entries add nothing to lse and get a zero gradient."""
+    S = _logits(N, V, dtype, seed=N + 3 * V)
+    masked = torch.zeros((N, V), dtype=torch.bool)
+    masked[0::2, : V // 3] = True
+    masked[1::2, 0::7] = True
+    S[masked] = float("-inf")
+    i = torch.arange(N, dtype=torch.int64)
+    t = V // 3 + (i * 7919) % (V - V // 3)
+    t = torch.where(t % 7 == 0, t + 1, t).clamp(max=V - 1)
+    t[t % 7 == 0] -= 2
+    t[::9] = IGN
+    assert not masked[i[t != IGN], t[t != IGN]].any()
+    ref = oracle.ce(S, t, IGN)
+    assert np.isfinite(ref["loss"])
+    lse = torch.empty(N, device=DEV)
+    loss, nval, dS = cuda_lib.flce_ce_fwd_bwd(S.to(DEV), t.to(DEV), IGN, sync=True, lse_out=lse)
+    assert int(nval.item()) == ref["n_valid"]
+    assert_loss(loss.item(), ref["loss"])
+    assert_loss(lse.cpu().numpy(), ref["lse"], "lse")
+    got = dS.float().cpu()
+    assert torch.isfinite(got).all()
+    assert (got[masked] == 0).all()
+    assert_grad(got.numpy(), ref["dS"], "dS")
+
+
 def test_ce_in_place_and_loss_only(cuda_lib):
     S = _logits(200, 3000, "bf16", seed=61)
     t = _targets(200, 3000, seed=62, ignore_num=10)

@@ -343,6 +343,30 @@ def test_ce_against_torch_cross_entropy():
     np.testing.assert_allclose(r["dS"].sum(axis=1), 0.0, atol=1e-15)
 
 
+def test_ce_masked_columns_equal_deleted_columns():
+    """A -inf (masked) logit is a column that is not there: CE over a row with
+    masked columns equals CE over the row with those columns deleted (loss,
+    lse, the visible gradient), and the masked columns' gradient is 0."""
+    g = torch.Generator().manual_seed(11)
+    S = torch.randn(12, 90, dtype=torch.float64, generator=g) * 2
+    keep = torch.ones(90, dtype=torch.bool)
+    keep[:30] = False
+    keep[45::4] = False
+    vis = torch.nonzero(keep).ravel()
+    t_vis = torch.randint(0, len(vis), (12,), generator=g)
+    t = vis[t_vis]
+    t[5] = IGN
+    t_vis[5] = IGN
+    Sm = S.clone()
+    Sm[:, ~keep] = float("-inf")
+    a = oracle.ce(Sm, t, IGN)
+    b = oracle.ce(S[:, keep].contiguous(), t_vis, IGN)
+    assert abs(a["loss"] - b["loss"]) <= 1e-14 * b["loss"]
+    np.testing.assert_allclose(a["lse"], b["lse"], rtol=1e-14)
+    np.testing.assert_allclose(a["dS"][:, keep.numpy()], b["dS"], rtol=1e-13, atol=1e-17)
+    assert (a["dS"][:, ~keep.numpy()] == 0).all()
+
+
 # --------------------------------------------- row / vocabulary subset functions
 def test_subset_functions_zero_weight_closed_forms():
     """W = 0 pins the sampled-row and sampled-dW-row functions on their own:
