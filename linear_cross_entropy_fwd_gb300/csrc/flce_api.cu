@@ -398,6 +398,12 @@ struct HostOverlap {
 
 // Rows of X that pass 1 keeps in L2 at a time (its M band), in bytes.
 constexpr size_t kPass1BandBytes = size_t{32} << 20;
+// dW walks H fastest inside bands of 8 H blocks: a wave of 76 pair tiles
+// then covers about 9.5 vocabulary blocks x 8 H blocks of the output, and
+// reads 9.5 slabs of G_c and half of X instead of 4.75 slabs and all of X.
+// At 8192 x 4096, chunk 4864: 358 -> 294 MB read per launch; same-box A/B
+// Llama-3 head +0.7 to +1.2% per call, Qwen2 head +0.6%, long context +1.0%.
+constexpr int32_t kDwHBand = 8;
 
 // The whole path on device pointers.  `ws` holds at least plan.total bytes.
 int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
@@ -549,6 +555,7 @@ int run_path(const Plan& P, const DeviceInfo& D, const void* X, const void* W,
           g.num_k_blk = static_cast<int32_t>((N + KE - 1) / KE);
           g.status = &sc->status;
           g.raster_n = 1;  // a slab of G_c rows with all of X stays in L2
+          g.n_band = kDwHBand;
           g.wait_operands = 1;  // G_c comes from the launch just before
           StoreParams sp{0, static_cast<int32_t>(c0), 0};
           const int grid = grid_for(static_cast<int64_t>(g.num_m_blk) * g.num_n_blk, units);

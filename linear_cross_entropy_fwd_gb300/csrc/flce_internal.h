@@ -39,6 +39,8 @@ struct GemmGrid {
   int32_t raster_n;    // 0: M index fastest in the tile order, 1: N index fastest
   int32_t m_band;      // raster_n = 0 and 0 < m_band < num_m_blk: the tile order
                        // covers bands of m_band M blocks one after the other
+  int32_t n_band;      // raster_n = 1 and 0 < n_band < num_n_blk: the same with
+                       // bands of n_band N blocks (N fastest inside a band)
   int32_t a_l2;        // L2 policy of operand loads: 0 normal, 1 evict first,
   int32_t b_l2;        // 2 evict last
   int32_t wait_operands;  // 1: an operand is written by the launch just before
@@ -54,7 +56,15 @@ struct GemmGrid {
 // band's rows of the M operand need to stay in L2, and the N operand streams
 // once per band.
 __host__ __device__ inline void tile_coords(const GemmGrid& g, int tile, int& m_blk, int& n_blk) {
-  if (g.raster_n) {
+  if (g.raster_n && g.n_band > 0 && g.n_band < g.num_n_blk) {
+    const int band_tiles = g.n_band * g.num_m_blk;
+    const int band = tile / band_tiles;
+    const int r = tile - band * band_tiles;
+    const int n0 = band * g.n_band;
+    const int cols = g.num_n_blk - n0 < g.n_band ? g.num_n_blk - n0 : g.n_band;
+    n_blk = n0 + r % cols;
+    m_blk = r / cols;
+  } else if (g.raster_n) {
     n_blk = tile % g.num_n_blk;
     m_blk = tile / g.num_n_blk;
   } else if (g.m_band > 0 && g.m_band < g.num_m_blk) {

@@ -124,8 +124,9 @@ def test_header_is_plain_c(tmp_path, std, lang):
 
 def test_tile_orders_cover_every_tile_once(tmp_path):
     """The GEMM launches' tile orders (M fastest, N fastest, M fastest in
-    bands of M blocks, ragged last band) map the tile indices one to one
-    onto the tile grid: the engine's own tile_coords, compiled for the host."""
+    bands of M blocks, N fastest in bands of N blocks, ragged last band) map
+    the tile indices one to one onto the tile grid: the engine's own
+    tile_coords, compiled for the host."""
     cxx = shutil.which("g++")
     if cxx is None:
         pytest.skip("no host compiler")
@@ -143,7 +144,8 @@ int main() {
       for (int raster : {0, 1})
         for (int band : {0, 1, 3, 8, 16, 18, 40}) {
           flce::GemmGrid g{};
-          g.num_m_blk = nm; g.num_n_blk = nn; g.raster_n = raster; g.m_band = band;
+          g.num_m_blk = nm; g.num_n_blk = nn; g.raster_n = raster;
+          (raster ? g.n_band : g.m_band) = band;
           std::vector<int> seen(nm * nn, 0);
           for (int t = 0; t < nm * nn; ++t) {
             int m, n;
