@@ -52,6 +52,11 @@ int combine_grid(int64_t N) {
 // block a fixed shuffle tree in double, then the last block to finish adds
 // the block sums in index order, so the result does not depend on scheduling.
 __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineParams p) {
+  // launched to overlap the previous launch's tail: its statistics are read
+  // only once it has completed; then the next launch may start (its loads of
+  // X and W begin, and it reads this kernel's results only after its own wait)
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * COMBINE_ROWS + lane;
   __shared__ float s_m[COMBINE_SPLIT][COMBINE_ROWS], s_l[COMBINE_SPLIT][COMBINE_ROWS];
@@ -175,15 +180,34 @@ cudaError_t launch_status_code(const Scalars* sc, int32_t* out, cudaStream_t s) 
   return cudaGetLastError();
 }
 
+// A launch that may begin while the previous one on the stream finishes
+// (programmatic dependent launch); the kernel waits before it reads.
+template <typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(Args...), unsigned blocks, unsigned threads,
+                              cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
-  combine_kernel<<<combine_grid(p.N), COMBINE_THREADS, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_overlapped(combine_kernel, static_cast<unsigned>(combine_grid(p.N)),
+                           COMBINE_THREADS, s, p);
 }
 
 // 8 elements per thread and iteration (two 16-byte loads, one 16-byte store).
 __global__ void convert_bf16_kernel(const float* __restrict__ src, uint4* __restrict__ dst,
                                     int64_t n8, const float* __restrict__ tail_src,
                                     uint16_t* __restrict__ tail_dst, int tail) {
+  grid_dependency_wait();  // the source is complete (overlapped launch)
+  grid_launch_dependents();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n8;
        k += stride) {
@@ -209,10 +233,9 @@ cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t n, int sms,
   const int64_t cap = static_cast<int64_t>(sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  convert_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      src, reinterpret_cast<uint4*>(dst), n8, src + n8 * 8,
-      reinterpret_cast<uint16_t*>(dst) + n8 * 8, tail);
-  return cudaGetLastError();
+  return launch_overlapped(convert_bf16_kernel, static_cast<unsigned>(blocks), 256u, s, src,
+                           reinterpret_cast<uint4*>(dst), n8, src + n8 * 8,
+                           reinterpret_cast<uint16_t*>(dst) + n8 * 8, tail);
 }
 
 // dst = (dst type)(src * scale), 8 elements per thread and iteration when both
