@@ -14,6 +14,9 @@
 // complete before its first global access, then lets the next launch start.
 // So when a launch starts, the one two before it has completed, and its
 // early units run their first tiles' MMAs in the previous launch's tail.
+// (Pass 2 follows the combine kernel, which lets it start at once: its
+// operands are the inputs X and W, and its epilogue waits for the combine,
+// which waits for pass 1.)
 //
 // Two shapes of the engine:
 //   PAIR = false  one CTA per 128 x 256 tile (cta_group::1), 4-stage ring of
