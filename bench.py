@@ -30,6 +30,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -153,13 +154,27 @@ KERNEL_SOURCES = {"logits_lse": _GEMM_SOURCES, "logits_grad": _GEMM_SOURCES,
                   "ce_rows_fp32": _SMALL_SOURCES}
 
 
-def kernel_source_hash(kind: str) -> str:
-    """Hash of the sources a kind of launch is built from."""
-    h = hashlib.sha256()
+def code_only(src: str) -> str:
+    """A C/C++/CUDA source without its comments and with its blank space
+    collapsed: the part that decides what the compiler builds.  (The sources
+    hashed here hold no comment markers inside string literals.)"""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
+def kernel_source_hash(kind: str, read=None) -> str:
+    """Hash of the code (comments aside) of the sources a kind of launch is
+    built from.  `read(name)` returns a source's text (default: the file in
+    the package's csrc)."""
     d = os.path.join(ROOT, "linear_cross_entropy_fwd_gb300", "csrc")
+    if read is None:
+        def read(name):
+            with open(os.path.join(d, name)) as fh:
+                return fh.read()
+    h = hashlib.sha256()
     for f in sorted(KERNEL_SOURCES[kind]):
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        h.update(f.encode() + code_only(read(f)).encode())
     return h.hexdigest()[:16]
 
 
