@@ -494,9 +494,6 @@ struct CeRowShape<4> {
   static constexpr int kKeepBytes = FLCE_CE_KEEP_FP32;
 };
 
-// Pass A over one CTA's vectors k, k + T, ... below hi of a row: (m, l) in the
-// log2 domain, kDepth 16-byte loads in flight per thread.  With KEEP each
-// vector read is also copied to keep[kk - keep_off].
 // Folds NV 16-byte vectors into (m, l): the vectors' max first, so one
 // rescale per call and then one exp2 and one add per element.
 template <int ELT, int NV>
