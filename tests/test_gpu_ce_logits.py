@@ -85,6 +85,27 @@ def test_ce_masked_logits(cuda_lib, N, V, dtype):
     assert_grad(got.numpy(), ref["dS"], "dS")
 
 
+@pytest.mark.parametrize("dtype,scale", [("bf16", -0.5), ("fp32", -2.0), ("bf16", 0.0),
+                                         ("bf16", 3.0)])
+def test_ce_grad_scale_signs(cuda_lib, dtype, scale):
+    """dS for a negative, a zero and a positive grad_scale.  A positive scale
+    is folded into the exponent; any other multiplies the softmax (the two
+    forms of the gradient pass).  Against the oracle's dS times the scale."""
+    N, V = 37, 20000
+    S = _logits(N, V, dtype, seed=71)
+    t = _targets(N, V, seed=72, ignore_num=10)
+    ref = oracle.ce(S, t, IGN)
+    loss, nval, dS = cuda_lib.flce_ce_fwd_bwd(S.to(DEV), t.to(DEV), IGN, sync=True,
+                                              grad_scale=scale)
+    assert int(nval.item()) == ref["n_valid"]
+    assert_loss(loss.item(), ref["loss"])
+    got = dS.float().cpu().numpy()
+    if scale == 0.0:
+        assert not got.any()
+    else:
+        assert_grad(got, scale * ref["dS"], f"dS x {scale}")
+
+
 def test_ce_in_place_and_loss_only(cuda_lib):
     S = _logits(200, 3000, "bf16", seed=61)
     t = _targets(200, 3000, seed=62, ignore_num=10)
