@@ -384,6 +384,7 @@ struct CeVec;
 template <>
 struct CeVec<2> {  // 8 bf16 per 16-byte access
   static constexpr int kPer = 8;
+  static constexpr uint32_t kMaskedWord = 0xFF80FF80u;  // two bf16 -inf
   __device__ static void unpack(const uint4& u, float* f) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -406,6 +407,7 @@ struct CeVec<2> {  // 8 bf16 per 16-byte access
 template <>
 struct CeVec<4> {  // 4 fp32 per 16-byte access
   static constexpr int kPer = 4;
+  static constexpr uint32_t kMaskedWord = 0xFF800000u;  // fp32 -inf
   __device__ static void unpack(const uint4& u, float* f) {
     f[0] = __uint_as_float(u.x);
     f[1] = __uint_as_float(u.y);
@@ -460,6 +462,11 @@ struct CeRowShape;
 // marked evict-first.  Same-box A/B (TB/s): bf16 keep 0 4.81, 64 KB 4.96,
 // 96 KB 4.97; fp32 keep 0 5.35, 64 KB 5.31, 96 KB 5.48.  With 96 KB the bf16
 // kernel reads 2.18 GB from DRAM for 2.10 GB of logits (2.50 GB without).
+// 96 KB is also the most the two CTAs of an SM can hold without losing L1:
+// at 2 x 96 KB the SM's shared memory fits a 196 KB carveout, above it the
+// SM takes the largest one and L1 drops from about 60 to 28 KB, too little
+// for the loads in flight.  Keeping 98.5 KB (an allocation of 98.5 or 106
+// KB) cost 15%, and 104 or 110 KB with L1::no_allocate loads 11%.
 // With the kept tail the loads in flight were swept again (same box, TB/s):
 //   bf16  split 1, 512 x 2: depth 3 4.88, 4 5.00, 5 4.96, 6 4.89;
 //         512 x 2 x 4 with 80 KB kept 4.97, 104 KB 4.68; 384 x 3 x 4 with
@@ -494,6 +501,37 @@ struct CeRowShape<4> {
   static constexpr int kKeepBytes = FLCE_CE_KEEP_FP32;
 };
 
+// 16-byte global loads (read-only path, or coherent) with an L2 eviction
+// policy that do not allocate the line in L1.
+__device__ __forceinline__ uint4 ld_nc_na_hint(const uint4* p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+
+__device__ __forceinline__ uint4 ld_na_hint(const uint4* p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy)
+               : "memory");
+  return v;
+}
+
+// Row loads of the two passes: bf16 rows without allocating in L1 (same-box
+// A/B +0.8 to +0.9% at 128256- and 152064-wide rows), fp32 rows as plain
+// loads (the same setting cost them 0.6%).
+template <int ELT>
+__device__ __forceinline__ uint4 ce_ld_first(const uint4* p, uint64_t pol) {
+  return ELT == 2 ? ld_nc_na_hint(p, pol) : ld_nc_hint(p, pol);
+}
+template <int ELT>
+__device__ __forceinline__ uint4 ce_ld_second(const uint4* p, uint64_t pol) {
+  return ELT == 2 ? ld_na_hint(p, pol) : ld_hint(p, pol);
+}
+
 // Folds NV 16-byte vectors into (m, l): the vectors' max first, so one
 // rescale per call and then one exp2 and one add per element.
 template <int ELT, int NV>
@@ -522,8 +560,9 @@ __device__ __forceinline__ void ce_stats_add(const uint4 (&u)[NV], float& m, flo
 }
 
 // Pass A over one CTA's vectors k, k + T, ... below hi of a row: (m, l) in the
-// log2 domain, kDepth 16-byte loads in flight per thread.  With KEEP each
-// vector read is also copied to keep[kk - keep_off].
+// log2 domain, kDepth 16-byte loads in flight per thread (also in the last,
+// partial batch).  With KEEP each vector read is also copied to
+// keep[kk - keep_off].
 template <int ELT, bool KEEP>
 __device__ __forceinline__ void ce_stats_vectors(const uint4* rv, int k, int hi, uint64_t pol,
                                                  uint4* keep, int keep_off, float& m, float& l) {
@@ -531,17 +570,27 @@ __device__ __forceinline__ void ce_stats_vectors(const uint4* rv, int k, int hi,
   for (; k + (D - 1) * T < hi; k += D * T) {
     uint4 u[D];
 #pragma unroll
-    for (int q = 0; q < D; ++q) u[q] = ld_nc_hint(rv + k + q * T, pol);
+    for (int q = 0; q < D; ++q) u[q] = ce_ld_first<ELT>(rv + k + q * T, pol);
     if (KEEP) {
 #pragma unroll
       for (int q = 0; q < D; ++q) keep[k + q * T - keep_off] = u[q];
     }
     ce_stats_add<ELT, D>(u, m, l);
   }
-  for (; k < hi; k += T) {
-    const uint4 u[1] = {ld_nc_hint(rv + k, pol)};
-    if (KEEP) keep[k - keep_off] = u[0];
-    ce_stats_add<ELT, 1>(u, m, l);
+  if (k < hi) {
+    // the passes that remain (fewer than kDepth): their loads in flight
+    // together; a vector past the end reads as -inf and adds nothing
+    constexpr uint32_t kM = CeVec<ELT>::kMaskedWord;
+    uint4 u[D];
+#pragma unroll
+    for (int q = 0; q < D; ++q)
+      u[q] = k + q * T < hi ? ce_ld_first<ELT>(rv + k + q * T, pol) : make_uint4(kM, kM, kM, kM);
+    if (KEEP) {
+#pragma unroll
+      for (int q = 0; q < D; ++q)
+        if (k + q * T < hi) keep[k + q * T - keep_off] = u[q];
+    }
+    ce_stats_add<ELT, D>(u, m, l);
   }
 }
 
@@ -582,15 +631,25 @@ __device__ __forceinline__ void ce_grad_vectors(const uint4* rv, uint4* ov, int 
     uint4 u[D];
 #pragma unroll
     for (int q = 0; q < D; ++q)
-      u[q] = FROM_KEEP ? keep[k + q * T - keep_off] : ld_hint(rv + k + q * T, pol);
+      u[q] = FROM_KEEP ? keep[k + q * T - keep_off] : ce_ld_second<ELT>(rv + k + q * T, pol);
 #pragma unroll
     for (int q = 0; q < D; ++q)
       st_hint(ov + k + q * T, ce_grad_vector<ELT, FOLD>(u[q], k + q * T, c, sc, one, tv, te),
               pol);
   }
-  for (; k < hi; k += T) {
-    const uint4 u = FROM_KEEP ? keep[k - keep_off] : ld_hint(rv + k, pol);
-    st_hint(ov + k, ce_grad_vector<ELT, FOLD>(u, k, c, sc, one, tv, te), pol);
+  if (k < hi) {  // the passes that remain (fewer than kDepth), loads in flight together
+    uint4 u[D];
+#pragma unroll
+    for (int q = 0; q < D; ++q) {
+      u[q] = make_uint4(0u, 0u, 0u, 0u);
+      if (k + q * T < hi)
+        u[q] = FROM_KEEP ? keep[k + q * T - keep_off] : ce_ld_second<ELT>(rv + k + q * T, pol);
+    }
+#pragma unroll
+    for (int q = 0; q < D; ++q)
+      if (k + q * T < hi)
+        st_hint(ov + k + q * T, ce_grad_vector<ELT, FOLD>(u[q], k + q * T, c, sc, one, tv, te),
+                pol);
   }
 }
 
