@@ -52,12 +52,14 @@ int combine_grid(int64_t N) {
 // block a fixed shuffle tree in double, then the last block to finish adds
 // the block sums in index order, so the result does not depend on scheduling.
 __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineParams p) {
-  // Launched to overlap the previous launch's tail.  The next launch (pass 2)
-  // may start at once: before its own wait it reads only X and W, which no
-  // kernel writes, and its first read of this kernel's results comes after
-  // that wait (which ends once this kernel, and so pass 1, has completed).
-  // So pass 2's first tiles can run on the units pass 1's last wave leaves
-  // idle.  This kernel reads pass 1's statistics after its own wait.
+  // Launched to overlap the previous launch's tail; it reads that launch's
+  // statistics only after its own wait.  The next launch may start at once.
+  // In the bf16 fused path that is pass 2: before its own wait it reads only
+  // X and W, which no kernel writes, and its first read of this kernel's
+  // results comes after that wait (which ends once this kernel, and so pass
+  // 1, has completed).  So pass 2's first tiles can run on the units pass
+  // 1's last wave leaves idle.  Every other launch that follows this kernel
+  // is a plain one, which starts only once this kernel has completed.
   grid_launch_dependents();
   grid_dependency_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
