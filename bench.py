@@ -412,7 +412,7 @@ def main():
     ap.add_argument("--shape", default=None,
                     help="N,H,V: a synthetic case of that size with the workload's recipe "
                          "(profiling runs; not a bench line)")
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=16)
     ap.add_argument("--vocab-chunk", type=int, default=0,
                     help="chunk width override (0 = the library's planner)")
     ap.add_argument("--ref-tokens", type=int, default=4)
