@@ -479,7 +479,10 @@ struct CeRowShape;
 // With the gradient pass cut to one comparison per vector for the target and
 // the scale folded into the exponent (about half the instructions per
 // logit), once more: bf16 512 x 2 depth 3 5.68, 4 5.87, 5 5.97, 6 5.55;
-// fp32 split 2, 512 x 2 depth 4 5.90, 5 6.06, 6 6.02, 8 5.97.
+// fp32 split 2, 512 x 2 depth 4 5.90, 5 6.06, 6 6.02, 8 5.97.  More rows
+// in flight with smaller kept tails, within the same carveout, lost again:
+// bf16 256 x 4 x 5 with 48 KB 4.36, 384 x 3 x 4 with 64 KB 5.55 (6.03 for
+// 512 x 2 x 5 on that box); fp32 4.14 and 5.48 (6.05).
 #ifndef FLCE_CE_KEEP_BF16
 #define FLCE_CE_KEEP_BF16 (96 * 1024)
 #endif
