@@ -682,9 +682,10 @@ __device__ __forceinline__ void ce_grad_row(const uint4* rv, uint4* ov, int v_lo
 // On the vector path each row's part is two ranges: [v_lo, v_keep), read
 // from global memory in both passes, and [v_keep, v_hi), at most kKeepBytes,
 // which pass A also copies to shared memory and pass B reads from there.
-// v_keep - v_lo is a whole number of passes of the CTA (kThreads vectors), so
-// each thread's vectors continue from one range into the next, and neither
-// range tests a vector's position against v_keep.  With a positive
+// Each range is walked from its own start (thread t takes its vectors t, t +
+// kThreads, ...), so neither tests a vector's position against v_keep, and
+// each thread reads back from shared memory exactly the vectors it put
+// there.  With a positive
 // scale sc, pass B computes 2^(S log2 e - (lse2 - log2 sc)) instead of
 // multiplying by sc, and corrects the target's element by -sc: the one
 // vector of the row that holds it is found by one comparison per vector.
@@ -712,11 +713,7 @@ __global__ void __launch_bounds__(CeRowShape<ELT>::kThreads, CeRowShape<ELT>::kC
   // vectors [v_keep, v_hi) stay in shared memory between the two passes
   // (only when there is a gradient pass and the rows are vectorised)
   int v_keep = v_hi;
-  if (vec && p.dlogits) {
-    const int over = v_hi - v_lo - kKeepVecs;
-    const int skip = over > 0 ? (over + kThreads - 1) / kThreads * kThreads : 0;
-    v_keep = v_lo + skip < v_hi ? v_lo + skip : v_hi;
-  }
+  if (vec && p.dlogits) v_keep = v_hi - kKeepVecs > v_lo ? v_hi - kKeepVecs : v_lo;
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) / SPLIT;
   const int64_t row_step = static_cast<int64_t>(gridDim.x) / SPLIT;
   const int64_t n = p.norm_count > 0 ? p.norm_count : p.sc->n_valid;
