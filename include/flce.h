@@ -181,11 +181,14 @@ FLCE_API int flce_fwd(const void* X, const void* W, const int64_t* target, int64
  *   dlogits [N, V], same type: dS = valid (softmax - onehot) * grad_scale / n;
  *   it may be the logits buffer itself (the gradient overwrites the logits,
  *   each element after it has been read); NULL computes the loss only.
+ * A -inf logit (a masked entry) adds nothing to lse and gets a zero
+ * gradient; a row needs one finite logit.  grad_scale may be of any sign;
+ * rows whose target is ignore_index get a zero gradient.
  * Optional outputs and error reporting as for flce_fwd_bwd_ex (lse_out,
  * loss_rows_out, loss_dev, n_valid_dev, status_dev, trace).  The scratch
  * space is 12 N bytes plus a few KB.  Memory traffic: one read of the logits
  * from HBM and, with a gradient, one write (the second read of each row
- * comes from L2).
+ * comes from shared memory for its last 96 KB, else from L2).
  */
 FLCE_API int flce_ce_fwd_bwd(const void* logits, const int64_t* target, int64_t N, int64_t V,
                              int64_t ignore_index, float* loss, void* dlogits,
